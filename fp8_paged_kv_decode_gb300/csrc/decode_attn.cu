@@ -1,0 +1,851 @@
+// decode_attn.cu -- paged decode attention over an FP8 e4m3 (or BF16) cache.
+//
+// What is computed: for each request r and query head i (KV head h = i / G)
+//     out[r][i] = sum_t softmax_t(sm_scale * q[r][i] . k_t) v_t
+// over the request's tokens, gathered through its CSR page table, with K/V
+// converted from the cache format as they are read.  The Cloudflare post
+// ("Smaller, faster, safer: running Kimi and GLM at scale", extracted on the
+// "Cloudflare Workers AI Optimizes Large Model Serving ..." page) stores the
+// cache as FP8 e4m3 instead of BF16 and notes the FP8 attention kernel has to
+// convert values as it reads them; requests aborted by the separate integrity
+// check are not read (fail closed).
+//
+// GB300 design (three launches, chained with programmatic dependent launch):
+//  1. plan (one CTA): tiles per request from seq_lens / abort mask / page
+//     table; prefix over requests; the first request of each worker warp.
+//     A "tile" is 32 tokens of one (request, KV head) unit.
+//  2. attention (persistent, one warp per CTA, grid = SMs x resident CTAs):
+//     the concatenation of all units' tiles is cut into equal contiguous
+//     ranges, one per warp (split-KV with perfect balance across the lognormal
+//     context mix).  Each warp streams its tiles through a private ring of
+//     shared-memory stages filled by 128B-swizzled TMA tensor copies (one 2-D
+//     box per page: K and V tiles of a (page, head) are contiguous in HBM).
+//     QK^T and PV run on the tensor cores as m16n8k16 MMAs with tokens on M
+//     and the G <= 8 query heads of the KV head on N; e4m3 codes become f16
+//     exactly in registers (the per-head scales fold into the logit factor and
+//     the output); softmax is online in fp32 with warp shuffles.  A warp that
+//     covers a whole unit writes the bf16 output directly; otherwise it writes
+//     an unnormalised fp32 partial (o, m, l) to the workspace.
+//  3. combine: merges the partials of each split unit (log-sum-exp rescale),
+//     zero-fills aborted / empty / invalid rows.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "fkv_common.cuh"
+
+namespace fkv {
+
+constexpr int kD = 128;
+constexpr int kTileT = 32;               // tokens per pipeline stage
+constexpr int kMaxGroup = 8;             // query heads sharing a KV head (MMA N)
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanSmemPrefix = 4096;    // requests whose prefix the plan searches in smem
+constexpr int kCombineWarps = 4;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;     // a copy that has not landed in 2 s has failed
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+
+struct AttnParams {
+    const __nv_bfloat16 *q;
+    const float *k_scale;
+    const float *v_scale;
+    const int32_t *indptr;
+    const int32_t *indices;
+    const int32_t *seq_lens;
+    const uint8_t *abort_mask;
+    const int64_t *prefix;     // [B+1] tile prefix over requests (tiles x Hkv)
+    const int32_t *warp_req;   // [NW] request holding each warp's first tile
+    float *part_o;             // [slots][G][D]
+    float2 *part_ml;           // [slots][G]  (m in log2 units, l; l < 0 marks an invalid unit)
+    __nv_bfloat16 *out;
+    uint32_t *err;
+    int B, Hq, Hkv, G, P, S, NW;
+    float sm_scale_log2;
+};
+
+template <bool kFp8>
+struct KvTraits;
+template <>
+struct KvTraits<true> {
+    static constexpr int kStages = 3;
+    static constexpr int kTileBytes = kTileT * kD;       // one K (or V) stage tile
+};
+template <>
+struct KvTraits<false> {
+    static constexpr int kStages = 3;
+    static constexpr int kTileBytes = kTileT * kD * 2;   // two 128-byte-wide halves
+};
+constexpr int kHalfBytes = kTileT * 128;
+
+template <bool kFp8>
+constexpr int attn_smem_bytes() {
+    return 1024 + KvTraits<kFp8>::kStages * 2 * KvTraits<kFp8>::kTileBytes + 64;
+}
+
+// ---------------------------------------------------------------------------
+// 1. plan
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPlanThreads)
+attn_plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ indptr,
+                 const uint8_t *__restrict__ abort_mask, int64_t nnz, int B, int Hkv, int S, int NW,
+                 int64_t *__restrict__ prefix, int32_t *__restrict__ warp_req) {
+    // let the attention grid start its prologue now
+    grid_dep_launch();
+    __shared__ int64_t s_warp_tot[kPlanThreads / 32];
+    __shared__ int64_t s_prefix[kPlanSmemPrefix + 1];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    int64_t carry = 0;
+    for (int base = 0; base < B; base += kPlanThreads) {
+        const int r = base + tid;
+        int64_t cnt = 0;
+        if (r < B) {
+            const int64_t sl = seq_lens[r];
+            const int64_t b = indptr[r], e = indptr[r + 1];
+            const bool alive = abort_mask == nullptr || abort_mask[r] == 0;
+            if (alive && sl > 0 && b >= 0 && e >= b && e <= nnz && (e - b) * S >= sl)
+                cnt = ((sl + kTileT - 1) / kTileT) * Hkv;
+        }
+        int64_t x = cnt;                                   // inclusive warp scan
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_warp_tot[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            int64_t v = s_warp_tot[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += y;
+            }
+            s_warp_tot[lane] = v;                           // inclusive over warps
+        }
+        __syncthreads();
+        const int64_t excl = carry + (wid ? s_warp_tot[wid - 1] : 0) + x - cnt;
+        if (r < B) {
+            prefix[r] = excl;
+            if (r < kPlanSmemPrefix) s_prefix[r] = excl;
+        }
+        carry += s_warp_tot[31];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        prefix[B] = carry;
+        if (B <= kPlanSmemPrefix) s_prefix[B] = carry;
+    }
+    __syncthreads();
+    const int64_t T = carry;
+    const bool in_smem = B <= kPlanSmemPrefix;
+    for (int w = tid; w < NW; w += kPlanThreads) {
+        const int64_t lo = static_cast<int64_t>(w) * T / NW;
+        int res = B;
+        if (lo < T) {
+            // largest r with prefix[r] <= lo (then prefix[r+1] > lo since lo < T)
+            int a = 0, z = B;                              // invariant: prefix[a] <= lo < prefix[z]
+            while (z - a > 1) {
+                const int mid = (a + z) >> 1;
+                const int64_t pm = in_smem ? s_prefix[mid] : prefix[mid];
+                if (pm <= lo) a = mid; else z = mid;
+            }
+            res = a;
+        }
+        warp_req[w] = res;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 2. split attention
+// ---------------------------------------------------------------------------
+struct Cursor {
+    int r, h, tt, nt;
+};
+
+__device__ __forceinline__ void cursor_init(Cursor &c, const AttnParams &p, int64_t x, int r) {
+    while (r < p.B - 1 && p.prefix[r + 1] <= x) ++r;
+    const int64_t base = p.prefix[r];
+    const int nt = static_cast<int>((p.prefix[r + 1] - base) / p.Hkv);
+    const int64_t rel = x - base;
+    c.r = r;
+    c.nt = nt;
+    c.h = static_cast<int>(rel / nt);
+    c.tt = static_cast<int>(rel - static_cast<int64_t>(c.h) * nt);
+}
+
+__device__ __forceinline__ void cursor_next(Cursor &c, const AttnParams &p) {
+    if (++c.tt < c.nt) return;
+    c.tt = 0;
+    if (++c.h < p.Hkv) return;
+    c.h = 0;
+    int r = c.r + 1;
+    while (r < p.B && p.prefix[r + 1] == p.prefix[r]) ++r;      // requests with no tiles
+    c.r = r;
+    c.nt = r < p.B ? static_cast<int>((p.prefix[r + 1] - p.prefix[r]) / p.Hkv) : 0;
+}
+
+__device__ __forceinline__ uint32_t lo16(uint32_t x) { return x & 0xFFFFu; }
+__device__ __forceinline__ uint32_t hi16(uint32_t x) { return x >> 16; }
+
+template <bool kFp8>
+__global__ void __launch_bounds__(32, 1)
+paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV) {
+    using Tr = KvTraits<kFp8>;
+    constexpr int NST = Tr::kStages;
+    constexpr int kTileBytes = Tr::kTileBytes;
+    constexpr int kStageBytes = 2 * kTileBytes;
+    constexpr uint32_t FULL = 0xffffffffu;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t bars = sbase + NST * kStageBytes;
+    const int lane = threadIdx.x;
+    const int g = lane >> 2, t = lane & 3;
+    const int w = blockIdx.x;
+    const int S = p.S, Hkv = p.Hkv, G = p.G;
+
+    if (lane == 0) {
+        for (int s = 0; s < NST; ++s) mbar_init(bars + 8 * s, 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
+    __syncwarp();
+    grid_dep_wait();                                   // plan results are visible
+
+    const int64_t T = p.prefix[p.B];
+    const int64_t lo = static_cast<int64_t>(w) * T / p.NW;
+    const int64_t hi = static_cast<int64_t>(w + 1) * T / p.NW;
+    if (lo >= hi) {
+        grid_dep_launch();
+        return;
+    }
+    const int64_t n_tiles = hi - lo;
+    const uint64_t policy = l2_policy_evict_first();
+
+    // ---------------- load side ----------------
+    Cursor L;
+    cursor_init(L, p, lo, p.warp_req[w]);
+    int pid_r = -1, pbase = 0, pidA = -1, pidB = -1, lseq = 0, lneed = 0;
+    int64_t lrow0 = 0;
+    uint32_t bad_bits = 0;                             // bit s: stage s has an out-of-pool page
+
+    auto fetch_ids = [&](int b) -> int {
+        const int pos = b + lane;
+        return pos < lneed ? __ldg(p.indices + lrow0 + pos) : -1;
+    };
+    auto page_id = [&](int pos) -> int {
+        if (pos < pbase || pos >= pbase + 64) {
+            pbase = pos & ~31;
+            pidA = fetch_ids(pbase);
+            pidB = fetch_ids(pbase + 32);
+        } else if (pos >= pbase + 32) {
+            pidA = pidB;
+            pbase += 32;
+            pidB = fetch_ids(pbase + 32);
+        }
+        return __shfl_sync(FULL, pidA, pos - pbase);
+    };
+    auto issue = [&](int stage) {
+        if (L.r != pid_r) {
+            pid_r = L.r;
+            lseq = __ldg(p.seq_lens + L.r);
+            lrow0 = __ldg(p.indptr + L.r);
+            lneed = (lseq + S - 1) / S;
+            pbase = -1000;
+        }
+        const int tok0 = L.tt * kTileT;
+        const int npg = S < kTileT ? kTileT / S : 1;
+        const int rows = S < kTileT ? S : kTileT;
+        const int pos0 = tok0 / S;
+        const int rowoff = S < kTileT ? 0 : tok0 % S;
+        int ids[2] = {-1, -1};
+        bool bad = false;
+        uint32_t bytes = 0;
+        for (int k = 0; k < npg; ++k) {
+            const int pos = pos0 + k;
+            if (pos >= lneed) break;                   // page beyond the request's last token
+            int id = page_id(pos);
+            if (id < 0 || id >= p.P) {                 // never dereference an id outside the pool
+                bad = true;
+                id = 0;
+            }
+            ids[k] = id;
+            bytes += 2u * rows * (kFp8 ? kD : 2 * kD);
+        }
+        bad_bits = (bad_bits & ~(1u << stage)) | (static_cast<uint32_t>(bad) << stage);
+        if (lane == 0) {
+            const uint32_t bar = bars + 8 * stage;
+            mbar_arrive_expect_tx(bar, bytes);
+            for (int k = 0; k < npg; ++k) {
+                if (ids[k] < 0) continue;
+                const uint32_t dk = sbase + stage * kStageBytes + k * rows * 128;
+                const uint32_t dv = dk + kTileBytes;
+                if (kFp8) {
+                    tma_load_4d(dk, &tmK, bar, 0, rowoff, L.h, ids[k], policy);
+                    tma_load_4d(dv, &tmV, bar, 0, rowoff, L.h, ids[k], policy);
+                } else {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        tma_load_4d(dk + half * kHalfBytes, &tmK, bar, half * 64, rowoff, L.h, ids[k], policy);
+                        tma_load_4d(dv + half * kHalfBytes, &tmV, bar, half * 64, rowoff, L.h, ids[k], policy);
+                    }
+                }
+            }
+        }
+    };
+
+    const int n_pro = n_tiles < NST ? static_cast<int>(n_tiles) : NST;
+    for (int i = 0; i < n_pro; ++i) {
+        issue(i);
+        cursor_next(L, p);
+    }
+
+    // ---------------- compute side ----------------
+    Cursor C;
+    cursor_init(C, p, lo, p.warp_req[w]);
+    uint32_t qb[8][2];
+    float cfac[2] = {0.f, 0.f};
+    float m[2], l[2];
+    float o[8][4];
+    int cseq = 0, seg_start = 0;
+    bool unit_bad = false;
+
+    for (int64_t i = 0; i < n_tiles; ++i) {
+        const int s = static_cast<int>(i % NST);
+        const uint32_t parity = static_cast<uint32_t>((i / NST) & 1);
+
+        if (i == 0 || C.tt == 0) {
+            // ---- new unit (r, h): queries, logit factors, fresh softmax state ----
+            cseq = __ldg(p.seq_lens + C.r);
+            seg_start = C.tt;
+            unit_bad = false;
+            m[0] = m[1] = -INFINITY;
+            l[0] = l[1] = 0.f;
+#pragma unroll
+            for (int a = 0; a < 8; ++a) o[a][0] = o[a][1] = o[a][2] = o[a][3] = 0.f;
+            const int64_t qrow = static_cast<int64_t>(C.r) * p.Hq + C.h * G + g;
+            const uint4 *q4 = reinterpret_cast<const uint4 *>(p.q) + qrow * (kD / 8);
+            uint4 qv[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                           make_uint4(0, 0, 0, 0)};
+            if (g < G) {
+                if (kFp8) {            // dims 32t .. 32t+31
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) qv[k] = __ldg(q4 + 4 * t + k);
+                } else {               // dims 16t .. 16t+15 and 64+16t .. 64+16t+15
+                    qv[0] = __ldg(q4 + 2 * t);
+                    qv[1] = __ldg(q4 + 2 * t + 1);
+                    qv[2] = __ldg(q4 + 8 + 2 * t);
+                    qv[3] = __ldg(q4 + 8 + 2 * t + 1);
+                }
+            }
+            const uint32_t qw[16] = {qv[0].x, qv[0].y, qv[0].z, qv[0].w, qv[1].x, qv[1].y, qv[1].z, qv[1].w,
+                                     qv[2].x, qv[2].y, qv[2].z, qv[2].w, qv[3].x, qv[3].y, qv[3].z, qv[3].w};
+            if (kFp8) {
+                // bf16 -> f16 with a power-of-two row scale so the row's largest
+                // magnitude lands in [2^14, 2^15): exact for every element within
+                // 2^-24 of it.  The scale is undone in the logit factor.
+                float amax = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    amax = fmaxf(amax, fabsf(__uint_as_float(qw[j] << 16)));
+                    amax = fmaxf(amax, fabsf(__uint_as_float(qw[j] & 0xFFFF0000u)));
+                }
+                amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 2));
+                int e = amax > 0.f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127 : 0;
+                e = max(-100, min(127, e));
+                const float sc = __uint_as_float(static_cast<uint32_t>(127 + 14 - e) << 23);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t w0 = qw[2 * ks], w1 = qw[2 * ks + 1];
+                    qb[ks][0] = pack_f16x2(__uint_as_float(w0 << 16) * sc, __uint_as_float(w0 & 0xFFFF0000u) * sc);
+                    qb[ks][1] = pack_f16x2(__uint_as_float(w1 << 16) * sc, __uint_as_float(w1 & 0xFFFF0000u) * sc);
+                }
+                const float ksc = __ldg(p.k_scale + C.h) * p.sm_scale_log2;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int ej = __shfl_sync(FULL, e, (2 * t + j) * 4);
+                    cfac[j] = ksc * __uint_as_float(static_cast<uint32_t>(127 + ej - 14) << 23);
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    qb[ks][0] = qw[2 * ks];
+                    qb[ks][1] = qw[2 * ks + 1];
+                }
+                cfac[0] = cfac[1] = p.sm_scale_log2;
+            }
+        }
+
+        // ---- wait for this stage's copies ----
+        if (!mbar_wait_bounded(bars + 8 * s, parity, kWaitLimitNs)) {
+            if (lane == 0) atomicOr(p.err, FKV_DEVERR_TIMEOUT);
+            // wind down: let every copy still in flight land before leaving
+            const int64_t last = i + NST < n_tiles ? i + NST : n_tiles;
+            for (int64_t j = i; j < last; ++j)
+                (void)mbar_wait_bounded(bars + 8 * static_cast<int>(j % NST),
+                                        static_cast<uint32_t>((j / NST) & 1), kDrainLimitNs);
+            return;
+        }
+        if ((bad_bits >> s) & 1u) {
+            if (!unit_bad && lane == 0) atomicOr(p.err, FKV_DEVERR_ATTN_PAGE);
+            unit_bad = true;
+        }
+        const uint32_t kbase = sbase + s * kStageBytes;
+        const uint32_t vbase = kbase + kTileBytes;
+        const int nvalid = min(kTileT, cseq - C.tt * kTileT);
+
+        if (nvalid < kTileT) {
+            // rows past the request's last token hold stale bytes: zero V there
+            // (K rows are masked out of the softmax instead)
+            const int nch = (kTileT - nvalid) * 8;
+#pragma unroll
+            for (int half = 0; half < (kFp8 ? 1 : 2); ++half)
+                for (int c = lane; c < nch; c += 32)
+                    st_shared_v4_zero(vbase + half * kHalfBytes + nvalid * 128 + c * 16);
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+
+        // ---- S^T = K Q^T : tokens on M (two 16-row tiles), heads on N ----
+        float sacc[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
+            const int ra = mt * 16 + g, rb = ra + 8;
+            if (kFp8) {
+                // this lane's 32 dims of rows ra, rb: 16-byte chunks 2t, 2t+1 (swizzled)
+                const uint4 a0 = ld_shared_v4(kbase + ra * 128 + (((2 * t) ^ (ra & 7)) << 4));
+                const uint4 a1 = ld_shared_v4(kbase + ra * 128 + (((2 * t + 1) ^ (ra & 7)) << 4));
+                const uint4 b0 = ld_shared_v4(kbase + rb * 128 + (((2 * t) ^ (rb & 7)) << 4));
+                const uint4 b1 = ld_shared_v4(kbase + rb * 128 + (((2 * t + 1) ^ (rb & 7)) << 4));
+                const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    mma_f16(sacc[mt], e4m3x2_to_f16x2(lo16(wa[ks])), e4m3x2_to_f16x2(lo16(wb[ks])),
+                            e4m3x2_to_f16x2(hi16(wa[ks])), e4m3x2_to_f16x2(hi16(wb[ks])), qb[ks][0], qb[ks][1]);
+                }
+            } else {
+                // dims 16t..16t+15 (half 0, chunks 2t, 2t+1) and 64+16t.. (half 1)
+                uint32_t wa[16], wb[16];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int half = k >> 1, c = 2 * t + (k & 1);
+                    const uint4 va = ld_shared_v4(kbase + half * kHalfBytes + ra * 128 + ((c ^ (ra & 7)) << 4));
+                    const uint4 vb = ld_shared_v4(kbase + half * kHalfBytes + rb * 128 + ((c ^ (rb & 7)) << 4));
+                    wa[4 * k] = va.x; wa[4 * k + 1] = va.y; wa[4 * k + 2] = va.z; wa[4 * k + 3] = va.w;
+                    wb[4 * k] = vb.x; wb[4 * k + 1] = vb.y; wb[4 * k + 2] = vb.z; wb[4 * k + 3] = vb.w;
+                }
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(sacc[mt], wa[2 * ks], wb[2 * ks], wa[2 * ks + 1], wb[2 * ks + 1], qb[ks][0], qb[ks][1]);
+            }
+        }
+
+        // ---- online softmax (log2 domain); columns are heads 2t, 2t+1 ----
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            if (mt * 16 + g >= nvalid) sacc[mt][0] = sacc[mt][1] = -INFINITY;
+            if (mt * 16 + g + 8 >= nvalid) sacc[mt][2] = sacc[mt][3] = -INFINITY;
+        }
+        float mx[2];
+        mx[0] = fmaxf(fmaxf(sacc[0][0], sacc[0][2]), fmaxf(sacc[1][0], sacc[1][2]));
+        mx[1] = fmaxf(fmaxf(sacc[0][1], sacc[0][3]), fmaxf(sacc[1][1], sacc[1][3]));
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(FULL, mx[j], 4));
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(FULL, mx[j], 8));
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(FULL, mx[j], 16));
+        }
+        float alpha[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float mnew = fmaxf(m[j], mx[j] * cfac[j]);
+            alpha[j] = ex2(m[j] - mnew);
+            m[j] = mnew;
+        }
+        float pr[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) pr[mt][c] = ex2(fmaf(sacc[mt][c], cfac[c & 1], -m[c & 1]));
+        l[0] = l[0] * alpha[0] + ((pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]));
+        l[1] = l[1] * alpha[1] + ((pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+            o[a][0] *= alpha[0];
+            o[a][2] *= alpha[0];
+            o[a][1] *= alpha[1];
+            o[a][3] *= alpha[1];
+        }
+        // P^T fragments: transpose (token, head) 8x8 blocks into (head, token)
+        uint32_t pb[2][2];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            const uint32_t x0 = kFp8 ? pack_f16x2(pr[mt][0], pr[mt][1]) : pack_bf16x2(pr[mt][0], pr[mt][1]);
+            const uint32_t x1 = kFp8 ? pack_f16x2(pr[mt][2], pr[mt][3]) : pack_bf16x2(pr[mt][2], pr[mt][3]);
+            pb[mt][0] = movmatrix_trans(x0);
+            pb[mt][1] = movmatrix_trans(x1);
+        }
+
+        // ---- O^T += V^T P^T : dims on M (8 blocks of 16), tokens on K ----
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            const int r0 = mt * 16 + 2 * t, r1 = r0 + 1, r2 = r0 + 8, r3 = r0 + 9;
+            if (kFp8) {
+                // dims 16g .. 16g+15 of four token rows (16-byte chunk g, swizzled)
+                const uint4 A = ld_shared_v4(vbase + r0 * 128 + ((g ^ (r0 & 7)) << 4));
+                const uint4 Bv = ld_shared_v4(vbase + r1 * 128 + ((g ^ (r1 & 7)) << 4));
+                const uint4 Cv = ld_shared_v4(vbase + r2 * 128 + ((g ^ (r2 & 7)) << 4));
+                const uint4 Dv = ld_shared_v4(vbase + r3 * 128 + ((g ^ (r3 & 7)) << 4));
+                const uint32_t a[4] = {A.x, A.y, A.z, A.w}, b[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
+                const uint32_t c[4] = {Cv.x, Cv.y, Cv.z, Cv.w}, d[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    // pair the same dim of tokens (r0, r1) and (r2, r3)
+                    const uint32_t ab0 = prmt(a[qq], b[qq], 0x5140), ab1 = prmt(a[qq], b[qq], 0x7362);
+                    const uint32_t cd0 = prmt(c[qq], d[qq], 0x5140), cd1 = prmt(c[qq], d[qq], 0x7362);
+                    mma_f16(o[2 * qq], e4m3x2_to_f16x2(lo16(ab0)), e4m3x2_to_f16x2(hi16(ab0)),
+                            e4m3x2_to_f16x2(lo16(cd0)), e4m3x2_to_f16x2(hi16(cd0)), pb[mt][0], pb[mt][1]);
+                    mma_f16(o[2 * qq + 1], e4m3x2_to_f16x2(lo16(ab1)), e4m3x2_to_f16x2(hi16(ab1)),
+                            e4m3x2_to_f16x2(lo16(cd1)), e4m3x2_to_f16x2(hi16(cd1)), pb[mt][0], pb[mt][1]);
+                }
+            } else {
+                // dims 8g..8g+7 (half 0, chunk g) and 64+8g.. (half 1, chunk g)
+                uint32_t a[8], b[8], c[8], d[8];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const uint32_t hb = vbase + half * kHalfBytes;
+                    const uint4 A = ld_shared_v4(hb + r0 * 128 + ((g ^ (r0 & 7)) << 4));
+                    const uint4 Bv = ld_shared_v4(hb + r1 * 128 + ((g ^ (r1 & 7)) << 4));
+                    const uint4 Cv = ld_shared_v4(hb + r2 * 128 + ((g ^ (r2 & 7)) << 4));
+                    const uint4 Dv = ld_shared_v4(hb + r3 * 128 + ((g ^ (r3 & 7)) << 4));
+                    a[4 * half] = A.x; a[4 * half + 1] = A.y; a[4 * half + 2] = A.z; a[4 * half + 3] = A.w;
+                    b[4 * half] = Bv.x; b[4 * half + 1] = Bv.y; b[4 * half + 2] = Bv.z; b[4 * half + 3] = Bv.w;
+                    c[4 * half] = Cv.x; c[4 * half + 1] = Cv.y; c[4 * half + 2] = Cv.z; c[4 * half + 3] = Cv.w;
+                    d[4 * half] = Dv.x; d[4 * half + 1] = Dv.y; d[4 * half + 2] = Dv.z; d[4 * half + 3] = Dv.w;
+                }
+#pragma unroll
+                for (int blk = 0; blk < 8; ++blk)
+                    mma_bf16(o[blk], prmt(a[blk], b[blk], 0x5410), prmt(a[blk], b[blk], 0x7632),
+                             prmt(c[blk], d[blk], 0x5410), prmt(c[blk], d[blk], 0x7632), pb[mt][0], pb[mt][1]);
+            }
+        }
+        __syncwarp();
+
+        // ---- refill this stage with the tile NST ahead ----
+        if (i + NST < n_tiles) {
+            issue(s);
+            cursor_next(L, p);
+        }
+
+        // ---- end of this warp's share of the unit ----
+        if (C.tt == C.nt - 1 || i == n_tiles - 1) {
+            float lt[2] = {l[0], l[1]};
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                lt[j] += __shfl_xor_sync(FULL, lt[j], 4);
+                lt[j] += __shfl_xor_sync(FULL, lt[j], 8);
+                lt[j] += __shfl_xor_sync(FULL, lt[j], 16);
+            }
+            const bool whole = seg_start == 0 && C.tt == C.nt - 1;
+            const int u = C.r * Hkv + C.h;
+            const float vsc = kFp8 ? __ldg(p.v_scale + C.h) : 1.f;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int hd = 2 * t + j;
+                if (hd >= G) continue;
+                // this lane's 16 dims of head hd, in ascending order
+                float v[16];
+#pragma unroll
+                for (int a = 0; a < 8; ++a) {
+                    v[2 * a] = o[a][j];
+                    v[2 * a + 1] = o[a][2 + j];
+                }
+                const int d0 = kFp8 ? 16 * g : 8 * g;          // first run of dims
+                const int d1 = kFp8 ? 16 * g + 8 : 64 + 8 * g; // second run (8 dims each)
+                if (whole) {
+                    const float f = unit_bad ? 0.f : vsc / lt[j];
+                    __nv_bfloat16 *orow = p.out + (static_cast<int64_t>(C.r) * p.Hq + C.h * G + hd) * kD;
+                    uint4 r0v, r1v;
+                    r0v.x = pack_bf16x2(v[0] * f, v[1] * f);
+                    r0v.y = pack_bf16x2(v[2] * f, v[3] * f);
+                    r0v.z = pack_bf16x2(v[4] * f, v[5] * f);
+                    r0v.w = pack_bf16x2(v[6] * f, v[7] * f);
+                    r1v.x = pack_bf16x2(v[8] * f, v[9] * f);
+                    r1v.y = pack_bf16x2(v[10] * f, v[11] * f);
+                    r1v.z = pack_bf16x2(v[12] * f, v[13] * f);
+                    r1v.w = pack_bf16x2(v[14] * f, v[15] * f);
+                    *reinterpret_cast<uint4 *>(orow + d0) = r0v;
+                    *reinterpret_cast<uint4 *>(orow + d1) = r1v;
+                } else {
+                    const int64_t slot = static_cast<int64_t>(u) + w;
+                    float *prow = p.part_o + (slot * G + hd) * kD;
+                    *reinterpret_cast<float4 *>(prow + d0) = make_float4(v[0], v[1], v[2], v[3]);
+                    *reinterpret_cast<float4 *>(prow + d0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+                    *reinterpret_cast<float4 *>(prow + d1) = make_float4(v[8], v[9], v[10], v[11]);
+                    *reinterpret_cast<float4 *>(prow + d1 + 4) = make_float4(v[12], v[13], v[14], v[15]);
+                    if (g == 0) p.part_ml[slot * G + hd] = make_float2(m[j], unit_bad ? -1.f : lt[j]);
+                }
+            }
+        }
+        cursor_next(C, p);
+    }
+    grid_dep_launch();
+}
+
+// ---------------------------------------------------------------------------
+// 3. combine split units
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int64_t warp_of_tile(int64_t x, int64_t T, int NW) {
+    // the warp w with floor(w*T/NW) <= x < floor((w+1)*T/NW)
+    const int64_t w = ((x + 1) * NW + T - 1) / T - 1;
+    return w < NW - 1 ? w : NW - 1;
+}
+
+__global__ void __launch_bounds__(32 * kCombineWarps)
+attn_combine_kernel(const AttnParams p, int kv_fp8) {
+    grid_dep_wait();                                  // partials are visible
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
+    if (row >= static_cast<int64_t>(p.B) * p.Hq) return;
+    const int r = static_cast<int>(row / p.Hq);
+    const int i = static_cast<int>(row % p.Hq);
+    const int h = i / p.G, hd = i % p.G;
+    uint2 *orow = reinterpret_cast<uint2 *>(p.out + row * kD) + lane;   // 4 bf16 per lane
+    const int64_t T = p.prefix[p.B];
+    const int64_t ntr = (p.prefix[r + 1] - p.prefix[r]) / p.Hkv;
+    if (ntr == 0) {                                   // aborted, empty or malformed: zero row
+        *orow = make_uint2(0u, 0u);
+        return;
+    }
+    const int64_t s0 = p.prefix[r] + h * ntr;
+    const int64_t wf = warp_of_tile(s0, T, p.NW), wl = warp_of_tile(s0 + ntr - 1, T, p.NW);
+    if (wf == wl) return;                             // one warp covered it and wrote it
+    const int64_t u = static_cast<int64_t>(r) * p.Hkv + h;
+    // warps with an empty range (possible when tiles < warps) wrote no partial
+    auto empty = [&](int64_t w) { return w * T / p.NW == (w + 1) * T / p.NW; };
+    float mmax = -INFINITY;
+    bool bad = false;
+    for (int64_t w = wf; w <= wl; ++w) {
+        if (empty(w)) continue;
+        const float2 ml = p.part_ml[(u + w) * p.G + hd];
+        bad |= ml.y < 0.f;
+        mmax = fmaxf(mmax, ml.x);
+    }
+    if (bad) {
+        *orow = make_uint2(0u, 0u);
+        return;
+    }
+    float ltot = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t w = wf; w <= wl; ++w) {
+        if (empty(w)) continue;
+        const float2 ml = p.part_ml[(u + w) * p.G + hd];
+        const float f = ex2(ml.x - mmax);
+        ltot += f * ml.y;
+        const float4 v = reinterpret_cast<const float4 *>(p.part_o + ((u + w) * p.G + hd) * kD)[lane];
+        acc.x += f * v.x;
+        acc.y += f * v.y;
+        acc.z += f * v.z;
+        acc.w += f * v.w;
+    }
+    const float sc = (kv_fp8 ? __ldg(p.v_scale + h) : 1.f) / ltot;
+    *orow = make_uint2(pack_bf16x2(acc.x * sc, acc.y * sc), pack_bf16x2(acc.z * sc, acc.w * sc));
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kMaxDev = 64;
+std::mutex g_mu;
+int g_ctas_per_sm[kMaxDev][2];       // [dev][kv_fp8]
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+template <bool kFp8>
+int ctas_per_sm() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    int &v = g_ctas_per_sm[dev][kFp8 ? 1 : 0];
+    if (!v) {
+        const int smem = attn_smem_bytes<kFp8>();
+        if (cudaFuncSetAttribute(paged_decode_attn_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem) != cudaSuccess)
+            return 0;
+        int nb = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, paged_decode_attn_kernel<kFp8>, 32, smem) !=
+                cudaSuccess ||
+            nb <= 0)
+            return 0;
+        v = nb < 16 ? nb : 16;
+    }
+    return v;
+}
+
+int grid_warps(bool fp8) {
+    const int sms = device_sm_count();
+    const int per = fp8 ? ctas_per_sm<true>() : ctas_per_sm<false>();
+    return sms * per;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+    size_t prefix, warp_req, part_ml, part_o, total;
+};
+
+WsLayout ws_layout(int B, int Hkv, int G, int NW) {
+    WsLayout L;
+    const size_t slots = static_cast<size_t>(B) * Hkv + NW;
+    L.prefix = 0;
+    L.warp_req = align256(L.prefix + sizeof(int64_t) * (static_cast<size_t>(B) + 1));
+    L.part_ml = align256(L.warp_req + sizeof(int32_t) * NW);
+    L.part_o = align256(L.part_ml + sizeof(float2) * slots * G);
+    L.total = align256(L.part_o + sizeof(float) * slots * G * kD);
+    return L;
+}
+
+bool make_kv_map(CUtensorMap *m, const void *base, bool fp8, int P, int Hkv, int S) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t es = fp8 ? 1 : 2;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(S),
+                                static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(P)};
+    const cuuint64_t strides[3] = {kD * es, static_cast<cuuint64_t>(S) * kD * es,
+                                   static_cast<cuuint64_t>(Hkv) * S * kD * es};
+    const cuuint32_t box[4] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(S < kTileT ? S : kTileT), 1u, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                           const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+}  // namespace
+}  // namespace fkv
+
+using namespace fkv;
+
+extern "C" size_t paged_decode_attn_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                                   int32_t head_dim, int32_t kv_dtype) {
+    if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;
+    if (head_dim != kD || (kv_dtype != FKV_KV_FP8_E4M3 && kv_dtype != FKV_KV_BF16)) return 0;
+    const int G = num_q_heads / num_kv_heads;
+    if (G > kMaxGroup) return 0;
+    const int NW = grid_warps(kv_dtype == FKV_KV_FP8_E4M3);
+    if (NW <= 0) return 0;
+    return ws_layout(batch, num_kv_heads, G, NW).total;
+}
+
+extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t num_q_heads, const void *k_cache,
+                                        const void *v_cache, int32_t kv_dtype, const float *k_scale,
+                                        const float *v_scale, int32_t num_pages, int32_t num_kv_heads,
+                                        int32_t page_size, int32_t head_dim, const int32_t *page_indptr,
+                                        const int32_t *page_indices, int64_t nnz, const int32_t *seq_lens,
+                                        const uint8_t *abort_mask, float sm_scale, void *out, void *workspace,
+                                        size_t workspace_bytes, void *stream) {
+    if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_pages <= 0 || nnz < 0) return FKV_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads) return FKV_ERR_INVALID_ARG;
+    if (kv_dtype != FKV_KV_FP8_E4M3 && kv_dtype != FKV_KV_BF16) return FKV_ERR_INVALID_ARG;
+    if (head_dim != kD) return FKV_ERR_UNSUPPORTED;
+    if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return FKV_ERR_UNSUPPORTED;
+    const int G = num_q_heads / num_kv_heads;
+    if (G > kMaxGroup) return FKV_ERR_UNSUPPORTED;
+    if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return FKV_ERR_INVALID_ARG;
+    if (batch == 0) return FKV_OK;
+    const bool fp8 = kv_dtype == FKV_KV_FP8_E4M3;
+    if (!q || !k_cache || !v_cache || !page_indptr || !seq_lens || !out || !workspace) return FKV_ERR_INVALID_ARG;
+    if (nnz > 0 && !page_indices) return FKV_ERR_INVALID_ARG;
+    if (fp8 && (!k_scale || !v_scale)) return FKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FKV_ERR_INVALID_ARG;
+    const int NW = grid_warps(fp8);
+    uint32_t *err = device_error_word();
+    if (NW <= 0 || !err) return FKV_ERR_CUDA;
+    const WsLayout wl = ws_layout(batch, num_kv_heads, G, NW);
+    if (workspace_bytes < wl.total) return FKV_ERR_INVALID_ARG;
+
+    CUtensorMap tmK, tmV;
+    if (!make_kv_map(&tmK, k_cache, fp8, num_pages, num_kv_heads, page_size) ||
+        !make_kv_map(&tmV, v_cache, fp8, num_pages, num_kv_heads, page_size))
+        return FKV_ERR_CUDA;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    AttnParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.indptr = page_indptr;
+    p.indices = page_indices;
+    p.seq_lens = seq_lens;
+    p.abort_mask = abort_mask;
+    p.prefix = reinterpret_cast<const int64_t *>(ws + wl.prefix);
+    p.warp_req = reinterpret_cast<const int32_t *>(ws + wl.warp_req);
+    p.part_ml = reinterpret_cast<float2 *>(ws + wl.part_ml);
+    p.part_o = reinterpret_cast<float *>(ws + wl.part_o);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.err = err;
+    p.B = batch;
+    p.Hq = num_q_heads;
+    p.Hkv = num_kv_heads;
+    p.G = G;
+    p.P = num_pages;
+    p.S = page_size;
+    p.NW = NW;
+    p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    attn_plan_kernel<<<1, kPlanThreads, 0, st>>>(seq_lens, page_indptr, abort_mask, nnz, batch, num_kv_heads,
+                                                   page_size, NW, reinterpret_cast<int64_t *>(ws + wl.prefix),
+                                                   reinterpret_cast<int32_t *>(ws + wl.warp_req));
+    FKV_CHECK_LAUNCH();
+    cudaError_t e;
+    if (fp8)
+        e = launch_pdl(paged_decode_attn_kernel<true>, dim3(NW), dim3(32), attn_smem_bytes<true>(), st, p, tmK, tmV);
+    else
+        e = launch_pdl(paged_decode_attn_kernel<false>, dim3(NW), dim3(32), attn_smem_bytes<false>(), st, p, tmK,
+                       tmV);
+    if (e != cudaSuccess) return FKV_ERR_CUDA;
+    const int64_t rows = static_cast<int64_t>(batch) * num_q_heads;
+    const unsigned cblocks = static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps);
+    e = launch_pdl(attn_combine_kernel, dim3(cblocks), dim3(32 * kCombineWarps), 0, st, p, fp8 ? 1 : 0);
+    if (e != cudaSuccess) return FKV_ERR_CUDA;
+    return FKV_OK;
+}

@@ -1,0 +1,78 @@
+// tag_check.cu -- the batched KV-page integrity check.
+//
+// "Kimi and GLM Reasoning Slimming: Hands-On Test", section "Giving Every
+// Physical Cache Page a 'Generation Number'", and the Cloudflare post's
+// integrity-checking section: every physical page carries a tag that changes
+// when the page is reallocated; each request records the pages and tags it
+// expects; before decode reads the cache the two are compared and a request
+// with any mismatch is aborted (fail closed).  The post runs the validation
+// as a separate batch pass, not fused into the attention kernel; this file is
+// that pass.
+//
+// One CTA per request: its threads stride over the request's CSR row,
+// gathering the live tag of each listed page (the tag array is small and stays
+// in L2), and the CTA ORs the per-thread verdicts with __syncthreads_or.  The
+// abort mask stays on the device for the attention call.
+#include "fkv_common.cuh"
+
+namespace fkv {
+
+constexpr int kCheckThreads = 128;
+
+__global__ void __launch_bounds__(kCheckThreads)
+kv_page_tag_check_kernel(const uint32_t *__restrict__ page_tags, int32_t num_pages,
+                         const int32_t *__restrict__ page_indptr, const int32_t *__restrict__ page_indices,
+                         const uint32_t *__restrict__ expected_tags, int64_t nnz,
+                         uint8_t *__restrict__ abort_mask) {
+    const int r = blockIdx.x;
+    const int64_t begin = __ldg(page_indptr + r);
+    const int64_t end = __ldg(page_indptr + r + 1);
+    int bad = 0;
+    if (begin < 0 || end < begin || end > nnz) {
+        bad = 1;                                            // malformed row: fail closed
+    } else {
+        int64_t j = begin + threadIdx.x;
+        // four independent gathers in flight per thread
+        for (; j + 3 * kCheckThreads < end; j += 4 * kCheckThreads) {
+            int32_t p[4];
+            uint32_t e[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                p[u] = __ldg(page_indices + j + u * kCheckThreads);
+                e[u] = __ldg(expected_tags + j + u * kCheckThreads);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (p[u] < 0 || p[u] >= num_pages) bad = 1;        // no such page
+                else bad |= __ldg(page_tags + p[u]) != e[u];     // stale or mismatched
+            }
+        }
+        for (; j < end; j += kCheckThreads) {
+            const int32_t p = __ldg(page_indices + j);
+            const uint32_t e = __ldg(expected_tags + j);
+            if (p < 0 || p >= num_pages) bad = 1;
+            else bad |= __ldg(page_tags + p) != e;
+        }
+    }
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) abort_mask[r] = bad ? 1 : 0;
+}
+
+}  // namespace fkv
+
+using namespace fkv;
+
+extern "C" fkv_status kv_page_tag_check(const uint32_t *page_tags, int32_t num_pages,
+                                        const int32_t *page_indptr, const int32_t *page_indices,
+                                        const uint32_t *expected_tags, int32_t batch, int64_t nnz,
+                                        uint8_t *abort_mask, void *stream) {
+    if (batch < 0 || nnz < 0 || num_pages < 0) return FKV_ERR_INVALID_ARG;
+    if (batch == 0) return FKV_OK;
+    if (!page_indptr || !abort_mask) return FKV_ERR_INVALID_ARG;
+    if (nnz > 0 && (!page_indices || !expected_tags)) return FKV_ERR_INVALID_ARG;
+    if (num_pages > 0 && !page_tags) return FKV_ERR_INVALID_ARG;
+    kv_page_tag_check_kernel<<<batch, kCheckThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        page_tags, num_pages, page_indptr, page_indices, expected_tags, nnz, abort_mask);
+    FKV_CHECK_LAUNCH();
+    return FKV_OK;
+}

@@ -245,3 +245,118 @@ def shard_requests(batch: int, rank: int, world: int) -> np.ndarray:
     contiguous, near-equal blocks; together they cover every request once."""
     bounds = [(batch * i) // world for i in range(world + 1)]
     return np.arange(bounds[rank], bounds[rank + 1], dtype=np.int64)
+
+
+# ----------------------------------------------------------------------------
+# full-size workloads drawn on the GPU
+# ----------------------------------------------------------------------------
+@dataclass
+class DeviceBatch:
+    """A workload whose bulk values are drawn on the GPU with a seeded torch
+    generator (host draws for shapes, lengths and the page table)."""
+    wl: Workload
+    ctx: np.ndarray
+    seq_lens: np.ndarray
+    pt: PageTable
+    tok_off: np.ndarray       # int64 [B] first row of each request in k_src / v_src
+    q: object                 # torch bf16 [B][Hq][D]
+    k_src: object             # torch bf16 [Ntok][Hkv][D]
+    v_src: object
+    slots_src: object         # torch int64 [Ntok]
+    k_new: object             # torch bf16 [B][Hkv][D]
+    v_new: object
+    slots_new: object         # torch int64 [B]
+    k_scale: np.ndarray       # float32 [Hkv]
+    v_scale: np.ndarray
+
+
+def _randn_bf16(torch, shape, gen, device, std=1.0, outliers=None, mult=1.0, chunk_rows=1 << 18):
+    """N(0, std^2) samples rounded to bf16, drawn in row chunks (bounded fp32 scratch);
+    ``outliers`` (kv_head, dim) columns are multiplied by ``mult`` before rounding."""
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    rows = shape[0]
+    for a in range(0, rows, chunk_rows):
+        b = min(rows, a + chunk_rows)
+        x = torch.randn((b - a,) + tuple(shape[1:]), generator=gen, device=device, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        if outliers is not None:
+            for h, d in outliers:
+                x[:, int(h), int(d)] *= mult
+        out[a:b] = x.to(torch.bfloat16)
+    return out
+
+
+def device_batch(wl: Workload, device, seed: int | None = None, ctx: np.ndarray | None = None) -> DeviceBatch:
+    import torch
+    seed = wl.seed if seed is None else seed
+    rng = np.random.default_rng(seed)
+    if ctx is None:
+        ctx = context_lengths(wl, rng)
+    ctx = np.asarray(ctx, dtype=np.int64)
+    seq = ctx + 1
+    pt = build_page_table(wl, seq, rng)
+    outl = outlier_channels(wl, rng)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    Hkv, D = wl.num_kv_heads, wl.head_dim
+    ntok = int(ctx.sum())
+    q = _randn_bf16(torch, (wl.batch, wl.num_q_heads, D), gen, device, std=wl.q_std)
+    k_src = _randn_bf16(torch, (ntok, Hkv, D), gen, device, outliers=outl, mult=wl.k_outlier_mult)
+    v_src = _randn_bf16(torch, (ntok, Hkv, D), gen, device)
+    k_new = _randn_bf16(torch, (wl.batch, Hkv, D), gen, device, outliers=outl, mult=wl.k_outlier_mult)
+    v_new = _randn_bf16(torch, (wl.batch, Hkv, D), gen, device)
+    if ntok:
+        k_amax = k_src.abs().amax(dim=(0, 2)).float().cpu().numpy()
+        v_amax = v_src.abs().amax(dim=(0, 2)).float().cpu().numpy()
+    else:
+        k_amax = v_amax = np.zeros(Hkv, np.float32)
+    tok_off = np.concatenate([[0], np.cumsum(ctx)[:-1]]).astype(np.int64)
+    return DeviceBatch(
+        wl=wl, ctx=ctx, seq_lens=seq.astype(np.int32), pt=pt, tok_off=tok_off, q=q, k_src=k_src, v_src=v_src,
+        slots_src=torch.from_numpy(prefill_slots(pt, wl.page_size, ctx)).to(device),
+        k_new=k_new, v_new=v_new,
+        slots_new=torch.from_numpy(slot_mapping(pt, wl.page_size, np.arange(wl.batch), ctx)).to(device),
+        k_scale=scale_from_amax(k_amax), v_scale=scale_from_amax(v_amax))
+
+
+@dataclass
+class CompactRequests:
+    """Selected requests of a batch, re-indexed onto a compact page pool so a
+    CPU check can rebuild their cache without the whole pool: page ``j`` of the
+    compact pool is original page ``orig_pages[j]``."""
+    reqs: np.ndarray
+    q: np.ndarray             # uint16 bf16 [n][Hq][D]
+    k_tokens: np.ndarray      # uint16 bf16 [Ntok'][Hkv][D] all cached + new tokens of the requests
+    v_tokens: np.ndarray
+    slots: np.ndarray         # int64 [Ntok'] compact slots
+    indptr: np.ndarray
+    indices: np.ndarray       # compact page ids
+    seq_lens: np.ndarray
+    orig_pages: np.ndarray    # int64 [n_pages]
+    num_pages: int
+
+
+def compact_requests(db: DeviceBatch, reqs) -> CompactRequests:
+    import torch
+    reqs = np.asarray(reqs, dtype=np.int64)
+    S = db.wl.page_size
+    orig, indptr, ks, vs, slots = [], [0], [], [], []
+    for r in reqs:
+        pages = db.pt.indices[db.pt.indptr[r]:db.pt.indptr[r + 1]].astype(np.int64)
+        base = len(orig)
+        orig.extend(pages.tolist())
+        indptr.append(indptr[-1] + pages.size)
+        a, n = int(db.tok_off[r]), int(db.ctx[r])
+        k = torch.cat([db.k_src[a:a + n], db.k_new[r:r + 1]]).view(torch.int16).cpu().numpy().view(np.uint16)
+        v = torch.cat([db.v_src[a:a + n], db.v_new[r:r + 1]]).view(torch.int16).cpu().numpy().view(np.uint16)
+        ks.append(k)
+        vs.append(v)
+        pos = np.arange(n + 1)
+        slots.append((base + pos // S) * S + pos % S)
+    q = db.q[torch.from_numpy(reqs).to(db.q.device)].view(torch.int16).cpu().numpy().view(np.uint16)
+    n_pages = len(orig)
+    return CompactRequests(
+        reqs=reqs, q=q, k_tokens=np.concatenate(ks), v_tokens=np.concatenate(vs), slots=np.concatenate(slots),
+        indptr=np.array(indptr, np.int32), indices=np.arange(n_pages, dtype=np.int32),
+        seq_lens=db.seq_lens[reqs].astype(np.int32), orig_pages=np.array(orig, np.int64), num_pages=n_pages)

@@ -1,0 +1,200 @@
+/*
+ * fkv.h -- C ABI of libfkv: FP8 paged-KV decode attention for sm_103a (GB300).
+ *
+ * The operations follow the description of Cloudflare's serving work in
+ * "Cloudflare Workers AI Optimizes Large Model Serving with KV Cache
+ * Quantization, Weight Compression, and Integrity Checks" (the extracted text
+ * of the post "Smaller, faster, safer: running Kimi and GLM at scale") and
+ * "Kimi and GLM Reasoning Slimming: Hands-On Test", section "Giving Every
+ * Physical Cache Page a 'Generation Number'":
+ *   - the KV cache is stored as FP8 e4m3 instead of BF16, halving its size;
+ *   - the FP8 attention kernel converts cache values as it reads them;
+ *   - every physical page has a tag that changes when it is reallocated; each
+ *     request records the (page, tag) pairs it expects; a separate batch check
+ *     (not fused into attention) runs before decode reads the cache, and a
+ *     mismatching request is aborted (fail closed); deployments that do not
+ *     enable the check pay nothing.
+ *
+ * Conventions for every call
+ *   - All array arguments are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or retains them.  `stream` is a cudaStream_t
+ *     passed as void* (NULL = the legacy default stream).
+ *   - Calls are asynchronous on `stream`: no host synchronisation, no
+ *     device-to-host copy.  Host-side argument checks return
+ *     FKV_ERR_INVALID_ARG / FKV_ERR_UNSUPPORTED synchronously and launch
+ *     nothing; a failed launch returns FKV_ERR_CUDA.
+ *   - Data-dependent problems found on the device never trap: they are
+ *     recorded in a sticky per-device error word (see fkv_device_error) and
+ *     the affected output is handled as documented per call.
+ *   - head_dim must be 128.  Cache, q and out must be 16-byte aligned.
+ *
+ * Layouts
+ *   KV pool (one per K and one per V, per layer):
+ *       [num_pages][num_kv_heads][page_size][head_dim]
+ *     one (page, head) tile is page_size * head_dim contiguous elements;
+ *     elements are e4m3 codes (1 byte) or bf16 (2 bytes).
+ *   Page table (CSR): page_indptr int32[batch + 1], page_indices int32[nnz];
+ *     token t of request r lives in page page_indices[page_indptr[r] + t /
+ *     page_size] at offset t % page_size.
+ *   Queries / outputs: bf16 [batch][num_q_heads][head_dim]; query head i
+ *     attends with KV head i / (num_q_heads / num_kv_heads).
+ */
+#ifndef FKV_H_
+#define FKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FKV_API __attribute__((visibility("default")))
+#else
+#define FKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FKV_OK = 0,
+    FKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment, small workspace */
+    FKV_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim != 128, group > 8, ...) */
+    FKV_ERR_CUDA = 3           /* a CUDA runtime call or launch failed */
+} fkv_status;
+
+typedef enum {
+    FKV_KV_FP8_E4M3 = 0,
+    FKV_KV_BF16 = 1
+} fkv_kv_dtype;
+
+/* Bits of the sticky device error word. */
+#define FKV_DEVERR_APPEND_SLOT   0x1u  /* kv_append_*: slot beyond the pool, token skipped */
+#define FKV_DEVERR_ATTN_PAGE     0x2u  /* paged_decode_attn: page id outside [0, num_pages), row zeroed */
+#define FKV_DEVERR_TIMEOUT       0x4u  /* a bounded wait on a copy gave up; the call's output is not valid */
+
+FKV_API const char *fkv_status_string(fkv_status s);
+
+/*
+ * kv_append_fp8 -- quantize new tokens' K and V to e4m3 and write them into
+ * their page slots.  (Cloudflare post: the cache is stored as FP8 e4m3 instead
+ * of BF16.)  For every token n with slot = slot_mapping[n] >= 0, KV head h and
+ * element d:
+ *     code = e4m3_rne_satfinite( fl32( fl32(x) / scale[h] ) )
+ * i.e. an IEEE round-to-nearest fp32 division followed by one
+ * round-to-nearest-even to e4m3; |values| > 448 and +-Inf saturate to +-448,
+ * NaN stays NaN.  The code goes to cache[slot / page_size][h][slot %
+ * page_size][d].
+ *
+ *   k_new, v_new   bf16 [n_tokens][num_kv_heads][head_dim]
+ *   slot_mapping   int64 [n_tokens]; < 0 means "padding, skip"
+ *   k_scale, v_scale  fp32 [num_kv_heads], positive and finite (this layer)
+ *   k_cache, v_cache  uint8 pools (layout above)
+ * A slot whose page is >= num_pages is skipped and sets FKV_DEVERR_APPEND_SLOT.
+ * Bytes outside the written slots are never touched.  n_tokens == 0 is a no-op.
+ */
+FKV_API fkv_status kv_append_fp8(const void *k_new, const void *v_new,
+                         const int64_t *slot_mapping, int32_t n_tokens,
+                         const float *k_scale, const float *v_scale,
+                         uint8_t *k_cache, uint8_t *v_cache,
+                         int32_t num_pages, int32_t num_kv_heads,
+                         int32_t page_size, int32_t head_dim, void *stream);
+
+/*
+ * kv_append_bf16 -- the BF16-cache counterpart of kv_append_fp8 (the
+ * comparison baseline the Cloudflare post measures against): the same
+ * placement, values stored unchanged.
+ */
+FKV_API fkv_status kv_append_bf16(const void *k_new, const void *v_new,
+                          const int64_t *slot_mapping, int32_t n_tokens,
+                          void *k_cache, void *v_cache,
+                          int32_t num_pages, int32_t num_kv_heads,
+                          int32_t page_size, int32_t head_dim, void *stream);
+
+/*
+ * kv_page_tag_check -- the separate batched integrity pass ("Kimi and GLM
+ * Reasoning Slimming: Hands-On Test", section "Giving Every Physical Cache
+ * Page a 'Generation Number'"; Cloudflare post, integrity checking).  For each
+ * request r:
+ *     abort_mask[r] = 1  if its CSR row is malformed (indptr[r] < 0,
+ *                        indptr[r+1] < indptr[r] or indptr[r+1] > nnz), or
+ *                        for any j in [indptr[r], indptr[r+1]):
+ *                        page_indices[j] outside [0, num_pages) or
+ *                        page_tags[page_indices[j]] != expected_tags[j]
+ *     abort_mask[r] = 0  otherwise.
+ *
+ *   page_tags      uint32 [num_pages]  live generation tags
+ *   page_indptr    int32 [batch + 1], page_indices int32 [nnz]
+ *   expected_tags  uint32 [nnz]  parallel to page_indices
+ *   abort_mask     uint8 [batch]  output, stays on the device; pass it to
+ *                  paged_decode_attn.  Not calling this function and passing
+ *                  abort_mask = NULL there is the no-tracker path.
+ * batch == 0 is a no-op.
+ */
+FKV_API fkv_status kv_page_tag_check(const uint32_t *page_tags, int32_t num_pages,
+                             const int32_t *page_indptr, const int32_t *page_indices,
+                             const uint32_t *expected_tags, int32_t batch, int64_t nnz,
+                             uint8_t *abort_mask, void *stream);
+
+/*
+ * paged_decode_attn_workspace_size -- bytes of device workspace that
+ * paged_decode_attn needs for this shape on the current device (it depends on
+ * the device's SM count).  Returns 0 for unsupported shapes.
+ */
+FKV_API size_t paged_decode_attn_workspace_size(int32_t batch, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t kv_dtype);
+
+/*
+ * paged_decode_attn -- decode-phase attention over the paged cache, values
+ * converted from the cache format as they are read (Cloudflare post: the FP8
+ * attention kernel converts values as it reads them).  For each request r and
+ * query head i (kv head h = i / G):
+ *     out[r][i] = sum_t softmax_t( sm_scale * q[r][i] . k_t ) v_t
+ * over the request's seq_lens[r] tokens, with k_t = code * k_scale[h] and
+ * v_t = code * v_scale[h] for FP8 (the bf16 values for BF16).
+ *
+ *   q              bf16 [batch][num_q_heads][head_dim]
+ *   k_cache, v_cache  pools (layout above) of dtype kv_dtype (fkv_kv_dtype)
+ *   k_scale, v_scale  fp32 [num_kv_heads] for FP8; ignored (may be NULL) for BF16
+ *   page_indptr, page_indices  the CSR page table; nnz = length of page_indices
+ *   seq_lens       int32 [batch]  tokens to attend per request
+ *   abort_mask     uint8 [batch] from kv_page_tag_check, or NULL (no tracker)
+ *   sm_scale       softmax scale, usually 1/sqrt(head_dim)
+ *   out            bf16 [batch][num_q_heads][head_dim]
+ *   workspace      device scratch of at least
+ *                  paged_decode_attn_workspace_size(...) bytes, 256-byte
+ *                  aligned; no initialisation needed; must not be shared by
+ *                  calls that overlap on the GPU.
+ * Fail closed: a request that is aborted, has a malformed CSR row (indptr[r]
+ * < 0, indptr[r+1] < indptr[r] or indptr[r+1] > nnz), has seq_lens[r] <= 0,
+ * has more tokens than its pages hold, or whose pages include an id outside
+ * [0, num_pages), gets an all-zero output row; its pages are not read (an
+ * out-of-range id is never dereferenced) and no other row is affected.
+ * Supported: head_dim 128, page_size in {16, 32, 64, 128}, group size
+ * num_q_heads / num_kv_heads in 1..8.
+ */
+FKV_API fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t num_q_heads,
+                             const void *k_cache, const void *v_cache, int32_t kv_dtype,
+                             const float *k_scale, const float *v_scale,
+                             int32_t num_pages, int32_t num_kv_heads,
+                             int32_t page_size, int32_t head_dim,
+                             const int32_t *page_indptr, const int32_t *page_indices,
+                             int64_t nnz, const int32_t *seq_lens, const uint8_t *abort_mask,
+                             float sm_scale, void *out,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * fkv_device_error -- read (and optionally clear) the sticky device error word
+ * of the current device.  Synchronises the device.  *flags receives the OR of
+ * FKV_DEVERR_* bits recorded since the last clear.
+ */
+FKV_API fkv_status fkv_device_error(uint32_t *flags, int32_t clear);
+
+/* Number of kernels one call launches (for launch accounting). */
+FKV_API int32_t fkv_kernels_per_call(const char *entry_point);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FKV_H_ */

@@ -88,7 +88,7 @@ class Oracle:
         lib.oracle_paged_decode_attn.restype = None
         lib.oracle_paged_decode_attn.argtypes = [
             P, i32, i32, P, P, i32, P, P, i32, i32, i32, i32,
-            P, P, P, P, ctypes.c_double, P, i32, P]
+            P, P, i64, P, P, ctypes.c_double, P, i32, P]
         self.lib = lib
         self.path = path
 
@@ -158,7 +158,7 @@ class Oracle:
         return out
 
     def paged_decode_attn(self, q, k_cache, v_cache, page_indptr, page_indices, seq_lens,
-                          sm_scale, k_scale=None, v_scale=None, abort_mask=None, rows=None):
+                          sm_scale, k_scale=None, v_scale=None, abort_mask=None, rows=None, nnz=None):
         """fp64 attention rows.  ``q`` is uint16 bf16 bits [B][Hq][D]; the caches
         are uint8 e4m3 codes (with ``k_scale/v_scale``) or uint16 bf16 bits,
         shaped [P][Hkv][S][D].  Returns [B][Hq][D], or [len(rows)][D] for a
@@ -184,7 +184,9 @@ class Oracle:
             n = rr.size
             out = np.zeros((n, D), dtype=np.float64)
         self.lib.oracle_paged_decode_attn(_ptr(q), B, Hq, _ptr(kc), _ptr(vc), int(fp8), _ptr(ks), _ptr(vs),
-                                          P, Hkv, S, D, _ptr(indptr), _ptr(indices), _ptr(sl), _ptr(am),
+                                          P, Hkv, S, D, _ptr(indptr), _ptr(indices),
+                                          int(indices.size if nnz is None else min(nnz, indices.size)),
+                                          _ptr(sl), _ptr(am),
                                           float(sm_scale), _ptr(rr), int(n), _ptr(out))
         return out
 

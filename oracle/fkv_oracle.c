@@ -43,9 +43,9 @@
  *   - GQA: query head i reads KV head i / G, G = Hq / Hkv.
  *   - tag check: a request aborts if any listed page id is outside [0, P),
  *     any live tag differs from the expected tag, or its CSR row is malformed.
- *   - attention: aborted, empty, or malformed requests (seq_len <= 0,
- *     seq_len > pages * S, or a page id read outside [0, P)) give an all-zero
- *     output row (fail closed).
+ *   - attention: aborted, empty, or malformed requests (a CSR row outside
+ *     [0, nnz], seq_len <= 0, seq_len > pages * S, or a page id read outside
+ *     [0, P)) give an all-zero output row (fail closed).
  */
 #include <math.h>
 #include <stdint.h>
@@ -277,7 +277,7 @@ void oracle_paged_decode_attn(const uint16_t *q, int32_t batch, int32_t num_q_he
                               const float *k_scale, const float *v_scale,
                               int32_t num_pages, int32_t num_kv_heads,
                               int32_t page_size, int32_t head_dim,
-                              const int32_t *page_indptr, const int32_t *page_indices,
+                              const int32_t *page_indptr, const int32_t *page_indices, int64_t nnz,
                               const int32_t *seq_lens, const uint8_t *abort_mask,
                               double sm_scale, const int32_t *rows, int32_t nrows,
                               double *out)
@@ -299,8 +299,10 @@ void oracle_paged_decode_attn(const uint16_t *q, int32_t batch, int32_t num_q_he
             o[d] = 0.0;
         if (abort_mask && abort_mask[r])
             continue;                                   /* aborted: zero row */
-        if (T <= 0 || npages < 0 || (int64_t)T > npages * page_size)
-            continue;                                   /* empty or malformed */
+        if (page_indptr[r] < 0 || npages < 0 || page_indptr[r + 1] > nnz)
+            continue;                                   /* malformed CSR row */
+        if (T <= 0 || (int64_t)T > npages * page_size)
+            continue;                                   /* empty, or more tokens than pages */
         for (int32_t t = 0; t < T && ok; t += page_size) {
             int32_t page = page_indices[page_indptr[r] + t / page_size];
             if (page < 0 || page >= num_pages)

@@ -430,6 +430,12 @@ def pin_attn_fail_closed(orc):
     for r in (0, 1, 3, 4):
         assert not got[r].any(), r
     assert np.array_equal(got[2], base[2])
+    # a CSR row that runs past the index list is malformed: zero row, nothing read
+    nnz = int(c["indptr"][-1]) - 1
+    got = orc.paged_decode_attn(c["q"], c["k"], c["v"], c["indptr"], c["indices"], c["seq"], sm,
+                                k_scale=c["ks"], v_scale=c["vs"], nnz=nnz)
+    assert not got[4].any()
+    assert np.array_equal(got[:4], base[:4])
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

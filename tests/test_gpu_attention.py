@@ -1,0 +1,133 @@
+"""paged_decode_attn on the GPU against the oracle, element by element, on
+shapes the oracle finishes in seconds: several tiles, ragged tails, every page
+size, every group size up to 8, splits across many warps, and the fail-closed
+cases."""
+import numpy as np
+import pytest
+
+from fp8_paged_kv_decode_gb300 import workloads as W
+from gpu_util import PagedCase, assert_close, bf16_out, dev
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    # (B, Hq, Hkv, S, seq)
+    (4, 8, 2, 16, [1, 17, 150, 300]),
+    (8, 64, 8, 64, [1, 31, 32, 33, 64, 65, 1000, 5000]),
+    (3, 8, 8, 32, [17, 200, 96]),            # G = 1
+    (3, 4, 2, 128, [300, 129, 5]),           # G = 2
+    (2, 16, 2, 64, [40000, 12345]),          # long: split over many warps
+    (5, 32, 8, 16, [4097, 1, 2, 3000, 16]),
+]
+
+
+@pytest.mark.parametrize("kv", ["fp8", "bf16"])
+@pytest.mark.parametrize("idx", range(len(SHAPES)), ids=[str(i) for i in range(len(SHAPES))])
+def test_matches_oracle(orc, kv, idx):
+    B, Hq, Hkv, S, seq = shape = SHAPES[idx]
+    case = PagedCase(orc, B, Hq, Hkv, S, seq, kv=kv, seed=100 + 2 * idx + (kv == "bf16"))
+    got = bf16_out(case.gpu())
+    assert_close(got, case.oracle(orc), "kv=%s shape=%s" % (kv, shape))
+
+
+@pytest.mark.parametrize("kv", ["fp8", "bf16"])
+def test_tiny_workload(orc, kv):
+    wl = W.WORKLOADS["tiny_gqa4"]
+    hb = W.host_batch(wl)
+    case = PagedCase(orc, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.page_size, hb.seq_lens, kv=kv, seed=11)
+    assert_close(bf16_out(case.gpu()), case.oracle(orc), "tiny_gqa4 " + kv)
+
+
+def test_peaky_softmax(orc):
+    """Logit std ~4 (q ~ 4 N(0,1)) over long contexts split across warps."""
+    case = PagedCase(orc, 2, 8, 1, 64, [20000, 7000], seed=3, q_std=4.0)
+    assert_close(bf16_out(case.gpu()), case.oracle(orc), "peaky")
+
+
+def test_fail_closed_rows(orc):
+    """Aborted, empty, over-long and bad-page requests give zero rows; the
+    other rows still match; the bad page id is never dereferenced and is
+    reported in the device error word."""
+    import fp8_paged_kv_decode_gb300 as fkv
+    B = 6
+    case = PagedCase(orc, B, 16, 2, 16, [100, 200, 300, 400, 500, 600], seed=4)
+    seq = case.seq.copy()
+    seq[1] = 0
+    seq[3] = 16 * ((400 + 15) // 16) + 1               # one token more than its pages hold
+    ind = case.indices.copy()
+    ind[case.indptr[4] + 7] = case.P + 1000               # outside the pool
+    am = np.array([1, 0, 0, 0, 0, 0], np.uint8)
+    fkv.device_error(clear=True)
+    got = bf16_out(case.gpu(abort_mask=am, seq=seq, indices=ind))
+    ref = case.oracle(orc, abort_mask=am, seq=seq, indices=ind)
+    for r in (0, 1, 3, 4):
+        assert not ref[r].any()
+        assert np.array_equal(got[r], np.zeros_like(got[r])), r
+    assert_close(got, ref, "fail-closed")
+    assert fkv.device_error() & fkv.DEVERR_ATTN_PAGE
+
+
+def test_no_tracker_path_equals_all_clear_mask(orc):
+    case = PagedCase(orc, 3, 8, 2, 64, [500, 70, 1], seed=5)
+    a = case.gpu()
+    b = case.gpu(abort_mask=np.zeros(3, np.uint8))
+    assert np.array_equal(a.cpu().numpy(), b.cpu().numpy())
+
+
+def test_abort_equals_absent_bytewise(orc):
+    """Aborting a request leaves every other row byte-identical to a batch
+    without that request (the split plan depends only on the live requests)."""
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    case = PagedCase(orc, 5, 32, 4, 64, [9000, 300, 20000, 4000, 1], seed=6)
+    am = np.array([0, 0, 1, 0, 0], np.uint8)
+    full = case.gpu(abort_mask=am).cpu()
+    keep = [0, 1, 3, 4]
+    # the same batch with request 2 removed from the page table and queries
+    indptr = [0]
+    ind = []
+    for r in keep:
+        pages = case.indices[case.indptr[r]:case.indptr[r + 1]]
+        ind.extend(pages.tolist())
+        indptr.append(len(ind))
+    q = dev(case.q[keep], dtype=torch.bfloat16)
+    out = torch.empty(len(keep), 32, 128, dtype=torch.bfloat16, device="cuda")
+    ws = fkv.alloc_workspace(len(keep), 32, 4)
+    fkv.paged_decode_attn(q, dev(case.kc), dev(case.vc), dev(np.array(indptr, np.int32)), dev(np.array(ind, np.int32)),
+                          dev(case.seq[keep]), case.sm, out, ws, k_scale=dev(case.k_scale), v_scale=dev(case.v_scale))
+    torch.cuda.synchronize()
+    assert np.array_equal(full[keep].view(torch.int16).numpy(), out.cpu().view(torch.int16).numpy())
+    assert not full[2].float().abs().sum()
+
+
+def test_page_permutation_invariant(orc):
+    """Moving pages to other physical slots changes nothing (bit for bit)."""
+    case = PagedCase(orc, 3, 16, 2, 32, [3000, 77, 1200], seed=7, spare=50)
+    base = case.gpu().cpu().numpy()
+    rng = np.random.default_rng(8)
+    perm = rng.permutation(case.P)
+    inv = np.argsort(perm)
+    got = case.gpu(indices=inv[case.indices].astype(np.int32), kc=case.kc[perm], vc=case.vc[perm]).cpu().numpy()
+    assert np.array_equal(base.view(np.int16), got.view(np.int16))
+
+
+def test_shared_pages_across_requests(orc):
+    """Two requests listing the same physical pages (a shared prefix) read the same data."""
+    case = PagedCase(orc, 2, 8, 2, 16, [160, 160], seed=9)
+    ind = case.indices.copy()
+    ind[case.indptr[1]:case.indptr[1] + 5] = ind[case.indptr[0]:case.indptr[0] + 5]
+    got = bf16_out(case.gpu(indices=ind))
+    assert_close(got, case.oracle(orc, indices=ind), "shared pages")
+
+
+def test_empty_batch_is_noop():
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    kc = torch.zeros(2, 1, 16, 128, dtype=torch.uint8, device="cuda")
+    q = torch.empty(0, 8, 128, dtype=torch.bfloat16, device="cuda")
+    s = torch.ones(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    i1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fkv.paged_decode_attn(q, kc, kc, i1, i1, i1[:0], 0.1, q, ws, k_scale=s, v_scale=s)
+    torch.cuda.synchronize()
+

@@ -1,0 +1,124 @@
+"""The five workloads at full size, through the same calls and launch
+configuration the benchmark times.  The oracle checks sampled requests (all
+their query heads) rebuilt from the bf16 source values it encodes itself;
+properties that hold at any size are checked on every row."""
+import numpy as np
+import pytest
+
+from fp8_paged_kv_decode_gb300 import workloads as W
+from gpu_util import assert_close, bf16_out, dev
+
+pytestmark = pytest.mark.gpu
+
+CASES = [("tiny_gqa4", "fp8"), ("tiny_gqa4", "bf16"), ("uniform_gqa8_8k", "fp8"), ("uniform_gqa8_8k", "bf16"),
+         ("pages_shaped_64req", "fp8"), ("pages_shaped_64req", "bf16"), ("long_ctx_131k", "fp8"),
+         ("integrity_256req", "fp8")]
+
+
+def run_step(db, kv):
+    """Populate the cache (bulk append), then one decode step: append the new
+    token, check tags, attend.  Returns device tensors."""
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    wl = db.wl
+    P, Hkv, S, D = db.pt.num_pages, wl.num_kv_heads, wl.page_size, wl.head_dim
+    fp8 = kv == "fp8"
+    dt = torch.uint8 if fp8 else torch.bfloat16
+    k_cache = torch.zeros(P, Hkv, S, D, dtype=dt, device="cuda")
+    v_cache = torch.zeros(P, Hkv, S, D, dtype=dt, device="cuda")
+    ks, vs = dev(db.k_scale), dev(db.v_scale)
+    if fp8:
+        fkv.kv_append_fp8(db.k_src, db.v_src, db.slots_src, ks, vs, k_cache, v_cache)
+        fkv.kv_append_fp8(db.k_new, db.v_new, db.slots_new, ks, vs, k_cache, v_cache)
+    else:
+        fkv.kv_append_bf16(db.k_src, db.v_src, db.slots_src, k_cache, v_cache)
+        fkv.kv_append_bf16(db.k_new, db.v_new, db.slots_new, k_cache, v_cache)
+    indptr, indices = dev(db.pt.indptr), dev(db.pt.indices)
+    mask = torch.empty(wl.batch, dtype=torch.uint8, device="cuda")
+    fkv.kv_page_tag_check(dev(db.pt.page_tags.view(np.int32)), indptr, indices,
+                          dev(db.pt.expected_tags.view(np.int32)), mask)
+    out = torch.full((wl.batch, wl.num_q_heads, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = fkv.alloc_workspace(wl.batch, wl.num_q_heads, Hkv, fkv.KV_FP8_E4M3 if fp8 else fkv.KV_BF16)
+    fkv.paged_decode_attn(db.q, k_cache, v_cache, indptr, indices, dev(db.seq_lens), 1.0 / np.sqrt(D), out, ws,
+                          k_scale=ks if fp8 else None, v_scale=vs if fp8 else None, abort_mask=mask)
+    torch.cuda.synchronize()
+    return k_cache, v_cache, mask, out
+
+
+def sample_requests(db, mask, n=3):
+    live = np.nonzero(mask == 0)[0]
+    dead = np.nonzero(mask != 0)[0]
+    pick = []
+    if live.size:
+        pick += [int(live[np.argmax(db.seq_lens[live])]), int(live[np.argmin(db.seq_lens[live])])]
+        rng = np.random.default_rng(0)
+        pick += [int(x) for x in rng.choice(live, size=min(n - 2, live.size), replace=False)]
+    if dead.size:
+        pick.append(int(dead[0]))
+    return np.unique(pick)
+
+
+@pytest.mark.parametrize("name,kv", CASES, ids=["%s-%s" % c for c in CASES])
+def test_fullsize_sampled_parity(orc, name, kv):
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    wl = W.WORKLOADS[name]
+    fkv.device_error(clear=True)
+    db = W.device_batch(wl, "cuda")
+    k_cache, v_cache, mask, out = run_step(db, kv)
+    mask_np = mask.cpu().numpy()
+    # the abort mask over the whole batch is bit-exact
+    want_mask = orc.kv_page_tag_check(db.pt.page_tags, db.pt.indptr, db.pt.indices, db.pt.expected_tags)
+    assert np.array_equal(mask_np, want_mask)
+    assert (want_mask.sum() > 0) == (wl.stale_frac > 0)
+    got_all = out.float()
+    # properties on every row: finite; aborted rows exactly zero
+    assert torch.isfinite(got_all).all()
+    if want_mask.any():
+        assert not got_all[torch.from_numpy(want_mask.astype(bool)).cuda()].abs().sum().item()
+    # sampled requests against the oracle
+    reqs = sample_requests(db, want_mask)
+    cr = W.compact_requests(db, reqs)
+    P2, Hkv, S, D = cr.num_pages, wl.num_kv_heads, wl.page_size, wl.head_dim
+    if kv == "fp8":
+        kc = np.zeros((P2, Hkv, S, D), np.uint8)
+        vc = np.zeros((P2, Hkv, S, D), np.uint8)
+        orc.kv_append_fp8(cr.k_tokens, cr.v_tokens, cr.slots, db.k_scale, db.v_scale, kc, vc)
+        gk = k_cache[torch.from_numpy(cr.orig_pages).cuda()].cpu().numpy()
+        gv = v_cache[torch.from_numpy(cr.orig_pages).cuda()].cpu().numpy()
+    else:
+        kc = np.zeros((P2, Hkv, S, D), np.uint16)
+        vc = np.zeros((P2, Hkv, S, D), np.uint16)
+        orc.kv_append_bf16(cr.k_tokens, cr.v_tokens, cr.slots, kc, vc)
+        pages = torch.from_numpy(cr.orig_pages).cuda()
+        gk = k_cache[pages].view(torch.int16).cpu().numpy().view(np.uint16)
+        gv = v_cache[pages].view(torch.int16).cpu().numpy().view(np.uint16)
+    # the appended bytes of every sampled token slot are bit-exact
+    pg, off = cr.slots // S, cr.slots % S
+    assert np.array_equal(gk[pg, :, off], kc[pg, :, off]) and np.array_equal(gv[pg, :, off], vc[pg, :, off])
+    # every head of short requests; 8 heads spread over the KV heads of long ones
+    Hq, G = wl.num_q_heads, wl.group
+    rows = []
+    for j, r in enumerate(cr.reqs):
+        heads = range(Hq) if db.seq_lens[r] <= 16384 else [k * (Hq // 8) + (k % G) for k in range(8)]
+        rows += [j * Hq + i for i in heads]
+    rows = np.array(rows, np.int32)
+    ref = orc.paged_decode_attn(cr.q, kc, vc, cr.indptr, cr.indices, cr.seq_lens, 1.0 / np.sqrt(D),
+                                k_scale=db.k_scale if kv == "fp8" else None,
+                                v_scale=db.v_scale if kv == "fp8" else None,
+                                abort_mask=want_mask[cr.reqs], rows=rows)
+    got = bf16_out(out[torch.from_numpy(cr.reqs).cuda()]).reshape(-1, D)[rows]
+    assert_close(got, ref, "%s %s requests %s" % (name, kv, cr.reqs.tolist()))
+    assert fkv.device_error() == 0
+
+
+def test_logit_spread_of_long_context_workload():
+    """long_ctx_131k draws q ~ 4 N(0,1) so q.k / sqrt(128) has std ~4 (peaky softmax)."""
+    import torch
+    wl = W.WORKLOADS["long_ctx_131k"]
+    db = W.device_batch(wl, "cuda", ctx=np.full(wl.batch, 4096))
+    q = db.q.float()[:, 0::wl.group]                         # one q head per KV head
+    k = db.k_src[:4096].float()                              # request 0, all KV heads
+    s = torch.einsum("hd,thd->th", q[0], k) / np.sqrt(wl.head_dim)
+    std = float(s.std())
+    assert 3.5 < std < 4.5, std

@@ -38,6 +38,7 @@ MUTANTS = {
     "attn_scale_k_by_v_scale": ("kd[(int64_t)t * D + d] = cache_value(k_cache, kv_is_fp8, base + d, k_scale, h);",
                                 "kd[(int64_t)t * D + d] = cache_value(k_cache, kv_is_fp8, base + d, v_scale, h);"),
     "attn_ignores_abort": ("if (abort_mask && abort_mask[r])", "if (0)"),
+    "attn_ignores_nnz": ("page_indptr[r + 1] > nnz)", "page_indptr[r + 1] > nnz + 1000000)"),
     "attn_last_token_dropped": ("for (int32_t t = 0; t < T; ++t) {\n            int64_t page",
                                 "for (int32_t t = 0; t < T - 1; ++t) {\n            int64_t page"),
 }
