@@ -1,0 +1,512 @@
+"""Benchmark: one decode step of the FP8 paged-KV path on the 64-request workload.
+
+A step is the whole hot path over one batch: append one new token per request
+(kv_append_fp8), the per-page generation-tag check (kv_page_tag_check), and
+paged decode attention (paged_decode_attn).  The workload is
+``pages_shaped_64req``: 64 concurrent requests, 64 query / 8 KV heads,
+head_dim 128, page 64, contexts lognormal (median 16384, sigma 0.8) clipped to
+[512, 131072], FP8 e4m3 KV (~2.9 GB read per step, far larger than L2, so no
+L2 flush is needed between steps).
+
+Prints one JSON line.  ``value`` is decode tokens/s (requests x steps / time,
+one layer); the roofline object is for the paged_decode_attn call, whose
+algorithmic bytes are the KV bytes of every attended token plus q, out and
+page ids.  The same step with a BF16 cache, the integrity-check overhead on
+``integrity_256req`` and the CPU oracle on a bounded sample are reported
+beside it.  ``--impl reference`` times the CPU oracle as the reference arm.
+
+Multi-GPU (torchrun): each rank runs its own replica batch (weak scaling), no
+collective on the data path; timing is max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attn tokens/s & HBM GB/s (% of 8 TB/s) at 64 req, FP8 vs BF16 KV"
+HEADLINE = "pages_shaped_64req"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--skip-extras", action="store_true", help="only the FP8 headline and e2e")
+    ap.add_argument("--cpu-requests", type=int, default=4, help="requests in the oracle's bounded sample")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# environment
+# ----------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peak_hbm():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode_attn.cu", "fkv_common.cuh"):
+        with open(os.path.join(ROOT, "fp8_paged_kv_decode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kv):
+    """DRAM bytes per paged_decode_attn call from a committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        e = t.get(kv)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return e
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.dev)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the step
+# ----------------------------------------------------------------------------
+class Step:
+    """Device state of one workload for one KV dtype: populated cache, page
+    table, tags and the per-step inputs."""
+
+    def __init__(self, db, kv, device):
+        import torch
+        import fp8_paged_kv_decode_gb300 as fkv
+        self.fkv, self.torch = fkv, torch
+        self.db, self.kv, self.device = db, kv, device
+        wl = db.wl
+        self.B, self.Hq, self.Hkv, self.S, self.D = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.page_size, wl.head_dim
+        P = db.pt.num_pages
+        self.fp8 = kv == "fp8"
+        dt = torch.uint8 if self.fp8 else torch.bfloat16
+        self.k_cache = torch.zeros(P, self.Hkv, self.S, self.D, dtype=dt, device=device)
+        self.v_cache = torch.zeros(P, self.Hkv, self.S, self.D, dtype=dt, device=device)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        self.k_scale, self.v_scale = t(db.k_scale), t(db.v_scale)
+        if self.fp8:
+            fkv.kv_append_fp8(db.k_src, db.v_src, db.slots_src, self.k_scale, self.v_scale, self.k_cache, self.v_cache)
+        else:
+            fkv.kv_append_bf16(db.k_src, db.v_src, db.slots_src, self.k_cache, self.v_cache)
+        self.indptr, self.indices = t(db.pt.indptr), t(db.pt.indices)
+        self.page_tags = t(db.pt.page_tags.view(np.int32))
+        self.expected = t(db.pt.expected_tags.view(np.int32))
+        self.seq_lens = t(db.seq_lens)
+        self.q, self.k_new, self.v_new, self.slots_new = db.q, db.k_new, db.v_new, db.slots_new
+        self.mask = torch.zeros(self.B, dtype=torch.uint8, device=device)
+        self.out = torch.empty(self.B, self.Hq, self.D, dtype=torch.bfloat16, device=device)
+        self.ws = fkv.alloc_workspace(self.B, self.Hq, self.Hkv, fkv.KV_FP8_E4M3 if self.fp8 else fkv.KV_BF16, device)
+        self.sm = 1.0 / np.sqrt(self.D)
+        torch.cuda.synchronize(device)
+
+    def append(self):
+        if self.fp8:
+            self.fkv.kv_append_fp8(self.k_new, self.v_new, self.slots_new, self.k_scale, self.v_scale, self.k_cache,
+                                   self.v_cache)
+        else:
+            self.fkv.kv_append_bf16(self.k_new, self.v_new, self.slots_new, self.k_cache, self.v_cache)
+
+    def check(self):
+        self.fkv.kv_page_tag_check(self.page_tags, self.indptr, self.indices, self.expected, self.mask)
+
+    def attend(self, with_mask=True):
+        self.fkv.paged_decode_attn(self.q, self.k_cache, self.v_cache, self.indptr, self.indices, self.seq_lens,
+                                   self.sm, self.out, self.ws, k_scale=self.k_scale if self.fp8 else None,
+                                   v_scale=self.v_scale if self.fp8 else None,
+                                   abort_mask=self.mask if with_mask else None)
+
+    def launches_per_step(self, with_check=True):
+        return (1 + (1 if with_check else 0) + self.fkv.kernels_per_call("paged_decode_attn"))
+
+    def attn_bytes(self):
+        """Algorithmic bytes of one paged_decode_attn call on the live requests:
+        K and V of every attended token, q and out, page ids and seq_lens."""
+        mask = self.mask.cpu().numpy()
+        live = mask == 0
+        seq = self.db.seq_lens.astype(np.int64)
+        es = 1 if self.fp8 else 2
+        kv = int((seq[live] * self.Hkv * self.D * 2 * es).sum())
+        pages = int(((seq[live] + self.S - 1) // self.S).sum())
+        qo = self.B * self.Hq * self.D * 2 * 2
+        return kv + qo + 4 * pages + 4 * self.B, int(seq[live].sum())
+
+    def timed(self, steps, warmup, with_check=True, sampler=None):
+        """Device time of ``steps`` steps and of the attention calls within them."""
+        torch = self.torch
+        stream = torch.cuda.current_stream(self.device)
+        for _ in range(warmup):
+            self.append()
+            if with_check:
+                self.check()
+            self.attend(with_check)
+        torch.cuda.synchronize(self.device)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize(self.device)
+        ctx = sampler if sampler is not None else _Null()
+        with ctx:
+            t0.record(stream)
+            for i in range(steps):
+                self.append()
+                if with_check:
+                    self.check()
+                ev[i][0].record(stream)
+                self.attend(with_check)
+                ev[i][1].record(stream)
+            t1.record(stream)
+            torch.cuda.synchronize(self.device)
+        barrier()
+        total_ms = t0.elapsed_time(t1)
+        attn_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+        return total_ms, attn_ms
+
+    def timed_e2e(self, steps, warmup):
+        """The same step through host buffers: every step copies its inputs from
+        pinned host memory and reads the output and abort mask back."""
+        torch = self.torch
+        stream = torch.cuda.current_stream(self.device)
+        pin = lambda x: x.cpu().pin_memory()
+        h_in = [pin(x) for x in (self.q, self.k_new, self.v_new, self.slots_new, self.seq_lens, self.indptr,
+                                 self.indices, self.expected, self.page_tags)]
+        d_in = [self.q, self.k_new, self.v_new, self.slots_new, self.seq_lens, self.indptr, self.indices,
+                self.expected, self.page_tags]
+        h_out = torch.empty_like(self.out, device="cpu").pin_memory()
+        h_mask = torch.empty_like(self.mask, device="cpu").pin_memory()
+        bi = sum(x.numel() * x.element_size() for x in h_in)
+        bo = h_out.numel() * h_out.element_size() + h_mask.numel() * h_mask.element_size()
+
+        def one():
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            self.append()
+            self.check()
+            self.attend(True)
+            h_out.copy_(self.out, non_blocking=True)
+            h_mask.copy_(self.mask, non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize(self.device)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        t0.record(stream)
+        for _ in range(steps):
+            one()
+        t1.record(stream)
+        torch.cuda.synchronize(self.device)
+        barrier()
+        return t0.elapsed_time(t1), bi, bo
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+_PG = None
+
+
+def barrier():
+    if _PG is not None:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x):
+    if _PG is None:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle on a bounded sample
+# ----------------------------------------------------------------------------
+def oracle_sample(db, kv, n_requests, start=0):
+    """Time the oracle's step (append the new token, check tags, attend, all
+    query heads) for ``n_requests`` requests of the batch, their cached context
+    pre-encoded by the oracle itself.  Returns (seconds, requests, sample text)."""
+    import oracle
+    from fp8_paged_kv_decode_gb300 import workloads as W
+    orc = oracle.default()
+    B = db.wl.batch
+    reqs = [(start + i) % B for i in range(n_requests)]
+    cr = W.compact_requests(db, reqs)
+    S, Hkv, D = db.wl.page_size, db.wl.num_kv_heads, db.wl.head_dim
+    fp8 = kv == "fp8"
+    dt = np.uint8 if fp8 else np.uint16
+    kc = np.zeros((cr.num_pages, Hkv, S, D), dt)
+    vc = np.zeros((cr.num_pages, Hkv, S, D), dt)
+    # context (all but each request's last token) is in the cache before the step
+    new_idx = np.cumsum(cr.seq_lens.astype(np.int64)) - 1
+    ctx_sel = np.ones(cr.slots.size, bool)
+    ctx_sel[new_idx] = False
+    if fp8:
+        orc.kv_append_fp8(cr.k_tokens[ctx_sel], cr.v_tokens[ctx_sel], cr.slots[ctx_sel], db.k_scale, db.v_scale, kc, vc)
+    else:
+        orc.kv_append_bf16(cr.k_tokens[ctx_sel], cr.v_tokens[ctx_sel], cr.slots[ctx_sel], kc, vc)
+    tags = db.pt.page_tags[cr.orig_pages]
+    exp = np.concatenate([db.pt.expected_tags[db.pt.indptr[r]:db.pt.indptr[r + 1]] for r in reqs])
+    t0 = time.perf_counter()
+    if fp8:
+        orc.kv_append_fp8(cr.k_tokens[new_idx], cr.v_tokens[new_idx], cr.slots[new_idx], db.k_scale, db.v_scale, kc, vc)
+    else:
+        orc.kv_append_bf16(cr.k_tokens[new_idx], cr.v_tokens[new_idx], cr.slots[new_idx], kc, vc)
+    mask = orc.kv_page_tag_check(tags, cr.indptr, cr.indices, exp)
+    orc.paged_decode_attn(cr.q, kc, vc, cr.indptr, cr.indices, cr.seq_lens, 1.0 / np.sqrt(D),
+                          k_scale=db.k_scale if fp8 else None, v_scale=db.v_scale if fp8 else None, abort_mask=mask)
+    dt_s = time.perf_counter() - t0
+    toks = int(cr.seq_lens.sum())
+    text = "%d of %d requests (%d context tokens, all %d query heads), one step each, 1 thread" % (
+        len(reqs), B, toks, db.wl.num_q_heads)
+    return dt_s, len(reqs), text
+
+
+# ----------------------------------------------------------------------------
+def workload_text(wl, db):
+    return ("%s: %d req, %d q / %d kv heads, head_dim %d, page %d, ctx %s, %d tokens attended per step"
+            % (wl.name, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.page_size, wl.ctx,
+               int(db.seq_lens.sum())))
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle as it stands, one bounded sample per step."""
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    import torch
+    from fp8_paged_kv_decode_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    device = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    db = W.device_batch(wl, device, seed=wl.seed)
+    times = []
+    for i in range(args.warmup + args.steps):
+        s, n, text = oracle_sample(db, "fp8", 1, start=i)
+        if i >= args.warmup:
+            times.append(s)
+    total = float(np.sum(times))
+    value = args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_text(wl, db), "step": "one request per step: append+check+attention"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "one request of the batch per step (cycling), all query heads, 1 thread"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    global _PG
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    world, rank, local = dist_env()
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        _PG = True
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import fp8_paged_kv_decode_gb300 as fkv
+    from fp8_paged_kv_decode_gb300 import workloads as W
+    if rank == 0 and not os.path.exists(fkv.library_path()):
+        from fp8_paged_kv_decode_gb300 import _build
+        _build.build()
+    barrier()
+    fkv.load_library()
+
+    wl = W.WORKLOADS[args.workload]
+    db = W.device_batch(wl, device, seed=wl.seed + rank)
+    fp8 = Step(db, "fp8", device)
+    fkv.device_error(clear=True)
+    sampler = ClockSampler(local)
+    total_ms, attn_ms = fp8.timed(args.steps, args.warmup, sampler=sampler)
+    total_ms = max_over_ranks(total_ms)
+    attn_ms = max_over_ranks(attn_ms)
+    ms_per_step = total_ms / args.steps
+    value = world * wl.batch * args.steps / (total_ms / 1e3)
+    attn_bytes, attended = fp8.attn_bytes()
+    peak, peak_kind = peak_hbm()
+    achieved = attn_bytes / (attn_ms / 1e3) / 1e9
+    traffic = recorded_traffic("fp8")
+
+    e2e_steps = max(10, args.steps // 4)
+    e2e_ms, bi, bo = fp8.timed_e2e(e2e_steps, max(3, args.warmup // 4))
+    e2e_ms = max_over_ranks(e2e_ms)
+    e2e_value = world * wl.batch * e2e_steps / (e2e_ms / 1e3)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 KV -> f16 MMA, f32 accumulate", "data": "synthetic",
+        "config": {"workload": workload_text(wl, db), "kv_dtype": "fp8_e4m3", "global_batch": world * wl.batch,
+                   "step": "kv_append_fp8 + kv_page_tag_check + paged_decode_attn (one layer)",
+                   "l2": "inputs larger than L2 (%.2f GB of KV read per step); no flush" % (attn_bytes / 1e9),
+                   "parallelism": "replicas x%d" % world},
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_attn (plan + split attention + combine)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind, "traffic": traffic["dram_bytes_per_call"] if traffic else None,
+                     "algorithmic_bytes": attn_bytes, "attn_ms": attn_ms,
+                     "frac_of_8tbs": achieved / 8000.0},
+        "attention_tokens_per_s": world * wl.batch / (attn_ms / 1e3),
+        "context_tokens_per_s": world * attended / (attn_ms / 1e3),
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+                "steps": e2e_steps},
+        "gpu_launches": args.steps * fp8.launches_per_step(),
+        "clocks": sampler.summary(),
+    }
+
+    if not args.skip_extras:
+        bf = Step(db, "bf16", device)
+        bms, battn = bf.timed(max(10, args.steps // 2), args.warmup)
+        bms, battn = max_over_ranks(bms), max_over_ranks(battn)
+        bbytes, _ = bf.attn_bytes()
+        bach = bbytes / (battn / 1e3) / 1e9
+        line["bf16_kv"] = {"value": world * wl.batch * max(10, args.steps // 2) / (bms / 1e3), "unit": "tokens/s",
+                           "ms_per_step": bms / max(10, args.steps // 2), "attn_ms": battn, "attn_gbs": bach,
+                           "frac": bach / peak, "algorithmic_bytes": bbytes}
+        line["fp8_over_bf16_attn_time"] = battn / attn_ms
+        del bf
+        torch.cuda.empty_cache()
+
+        iw = W.WORKLOADS["integrity_256req"]
+        idb = W.device_batch(iw, device, seed=iw.seed + rank)
+        ist = Step(idb, "fp8", device)
+        n_i = max(50, args.steps // 4)
+        on_ms, _ = ist.timed(n_i, args.warmup, with_check=True)
+        off_ms, _ = ist.timed(n_i, args.warmup, with_check=False)
+        # the check kernel alone
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(5):
+            ist.check()
+        ev0.record()
+        for _ in range(n_i):
+            ist.check()
+        ev1.record()
+        torch.cuda.synchronize()
+        chk_us = 1e3 * ev0.elapsed_time(ev1) / n_i
+        line["integrity_check"] = {
+            "workload": workload_text(iw, idb), "aborted_requests": int(ist.mask.sum().item()),
+            "step_ms_with_check": on_ms / n_i, "step_ms_without_check": off_ms / n_i,
+            "overhead_pct": 100.0 * (on_ms - off_ms) / off_ms, "check_kernel_us": chk_us,
+            "check_share_of_step_pct": 100.0 * chk_us / (1e3 * on_ms / n_i)}
+        del ist, idb
+        torch.cuda.empty_cache()
+
+    derr = fkv.device_error()
+    if derr:
+        line["device_error"] = derr
+    if rank == 0:
+        t0 = time.perf_counter()
+        s, n, text = oracle_sample(db, "fp8", args.cpu_requests)
+        line["cpu_baseline"] = {"value": n / s, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": text}
+        print(json.dumps(line), flush=True)
+    if _PG is not None:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

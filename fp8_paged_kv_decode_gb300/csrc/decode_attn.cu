@@ -482,14 +482,29 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             o[a][1] *= alpha[1];
             o[a][3] *= alpha[1];
         }
-        // P^T fragments: transpose (token, head) 8x8 blocks into (head, token)
-        uint32_t pb[2][2];
+        // P^T fragments: transpose (token, head) 8x8 blocks into (head, token).
+        // FP8: P in f16 (11-bit significand).  BF16: the MMA needs bf16 P, whose
+        // 8-bit significand alone would cost up to 2^-9 |v| in the output, so P
+        // is split into bf16 hi + lo parts and PV runs on both (16 bits).
+        uint32_t pb[2][2], pl[2][2];
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
-            const uint32_t x0 = kFp8 ? pack_f16x2(pr[mt][0], pr[mt][1]) : pack_bf16x2(pr[mt][0], pr[mt][1]);
-            const uint32_t x1 = kFp8 ? pack_f16x2(pr[mt][2], pr[mt][3]) : pack_bf16x2(pr[mt][2], pr[mt][3]);
-            pb[mt][0] = movmatrix_trans(x0);
-            pb[mt][1] = movmatrix_trans(x1);
+            if (kFp8) {
+                pb[mt][0] = movmatrix_trans(pack_f16x2(pr[mt][0], pr[mt][1]));
+                pb[mt][1] = movmatrix_trans(pack_f16x2(pr[mt][2], pr[mt][3]));
+                pl[mt][0] = pl[mt][1] = 0u;
+            } else {
+                const uint32_t h0 = pack_bf16x2(pr[mt][0], pr[mt][1]);
+                const uint32_t h1 = pack_bf16x2(pr[mt][2], pr[mt][3]);
+                const uint32_t l0 = pack_bf16x2(pr[mt][0] - __uint_as_float(h0 << 16),
+                                                pr[mt][1] - __uint_as_float(h0 & 0xFFFF0000u));
+                const uint32_t l1 = pack_bf16x2(pr[mt][2] - __uint_as_float(h1 << 16),
+                                                pr[mt][3] - __uint_as_float(h1 & 0xFFFF0000u));
+                pb[mt][0] = movmatrix_trans(h0);
+                pb[mt][1] = movmatrix_trans(h1);
+                pl[mt][0] = movmatrix_trans(l0);
+                pl[mt][1] = movmatrix_trans(l1);
+            }
         }
 
         // ---- O^T += V^T P^T : dims on M (8 blocks of 16), tokens on K ----
@@ -530,9 +545,12 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                     d[4 * half] = Dv.x; d[4 * half + 1] = Dv.y; d[4 * half + 2] = Dv.z; d[4 * half + 3] = Dv.w;
                 }
 #pragma unroll
-                for (int blk = 0; blk < 8; ++blk)
-                    mma_bf16(o[blk], prmt(a[blk], b[blk], 0x5410), prmt(a[blk], b[blk], 0x7632),
-                             prmt(c[blk], d[blk], 0x5410), prmt(c[blk], d[blk], 0x7632), pb[mt][0], pb[mt][1]);
+                for (int blk = 0; blk < 8; ++blk) {
+                    const uint32_t A0 = prmt(a[blk], b[blk], 0x5410), A1 = prmt(a[blk], b[blk], 0x7632);
+                    const uint32_t A2 = prmt(c[blk], d[blk], 0x5410), A3 = prmt(c[blk], d[blk], 0x7632);
+                    mma_bf16(o[blk], A0, A1, A2, A3, pb[mt][0], pb[mt][1]);
+                    mma_bf16(o[blk], A0, A1, A2, A3, pl[mt][0], pl[mt][1]);
+                }
             }
         }
         __syncwarp();

@@ -69,9 +69,10 @@ def test_fail_closed_rows(orc):
 
 def test_no_tracker_path_equals_all_clear_mask(orc):
     case = PagedCase(orc, 3, 8, 2, 64, [500, 70, 1], seed=5)
-    a = case.gpu()
-    b = case.gpu(abort_mask=np.zeros(3, np.uint8))
-    assert np.array_equal(a.cpu().numpy(), b.cpu().numpy())
+    import torch
+    a = case.gpu().view(torch.int16).cpu().numpy()
+    b = case.gpu(abort_mask=np.zeros(3, np.uint8)).view(torch.int16).cpu().numpy()
+    assert np.array_equal(a, b)
 
 
 def test_abort_equals_absent_bytewise(orc):
@@ -102,13 +103,14 @@ def test_abort_equals_absent_bytewise(orc):
 
 def test_page_permutation_invariant(orc):
     """Moving pages to other physical slots changes nothing (bit for bit)."""
+    import torch
     case = PagedCase(orc, 3, 16, 2, 32, [3000, 77, 1200], seed=7, spare=50)
-    base = case.gpu().cpu().numpy()
+    base = case.gpu().view(torch.int16).cpu().numpy()
     rng = np.random.default_rng(8)
     perm = rng.permutation(case.P)
     inv = np.argsort(perm)
-    got = case.gpu(indices=inv[case.indices].astype(np.int32), kc=case.kc[perm], vc=case.vc[perm]).cpu().numpy()
-    assert np.array_equal(base.view(np.int16), got.view(np.int16))
+    got = case.gpu(indices=inv[case.indices].astype(np.int32), kc=case.kc[perm], vc=case.vc[perm])
+    assert np.array_equal(base, got.view(torch.int16).cpu().numpy())
 
 
 def test_shared_pages_across_requests(orc):

@@ -100,7 +100,7 @@ def test_fullsize_sampled_parity(orc, name, kv):
     Hq, G = wl.num_q_heads, wl.group
     rows = []
     for j, r in enumerate(cr.reqs):
-        heads = range(Hq) if db.seq_lens[r] <= 16384 else [k * (Hq // 8) + (k % G) for k in range(8)]
+        heads = range(Hq) if db.seq_lens[r] <= 16384 else [k * (Hq // 8) + (k % (Hq // 8)) for k in range(8)]
         rows += [j * Hq + i for i in heads]
     rows = np.array(rows, np.int32)
     ref = orc.paged_decode_attn(cr.q, kc, vc, cr.indptr, cr.indices, cr.seq_lens, 1.0 / np.sqrt(D),
