@@ -250,6 +250,38 @@ class Step:
         attn_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
         return total_ms, attn_ms
 
+    def graph(self, with_check=True, checks_only=0):
+        """One step (or ``checks_only`` back-to-back checks) captured in a CUDA
+        graph, so host launch cost is out of the measurement."""
+        torch = self.torch
+        body = (lambda: [self.check() for _ in range(checks_only)]) if checks_only else \
+            (lambda: (self.append(), self.check() if with_check else None, self.attend(with_check)))
+        body()                                    # one-time set-up happens outside the capture
+        torch.cuda.synchronize(self.device)
+        s = torch.cuda.Stream(self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            body()
+        torch.cuda.synchronize(self.device)
+        return g
+
+    def timed_graph(self, steps, warmup, with_check=True, checks_only=0):
+        torch = self.torch
+        g = self.graph(with_check, checks_only)
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize(self.device)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        t0.record()
+        for _ in range(steps):
+            g.replay()
+        t1.record()
+        torch.cuda.synchronize(self.device)
+        barrier()
+        return t0.elapsed_time(t1)
+
     def timed_e2e(self, steps, warmup):
         """The same step through host buffers: every step copies its inputs from
         pinned host memory and reads the output and abort mask back."""
@@ -470,28 +502,35 @@ def main():
         del bf
         torch.cuda.empty_cache()
 
+        # integrity check cost: the 0%-stale variant of integrity_256req with
+        # and without the check, each step captured in a CUDA graph
+        import dataclasses
         iw = W.WORKLOADS["integrity_256req"]
-        idb = W.device_batch(iw, device, seed=iw.seed + rank)
+        iw0 = dataclasses.replace(iw, stale_frac=0.0)
+        idb = W.device_batch(iw0, device, seed=iw.seed + rank)
         ist = Step(idb, "fp8", device)
-        n_i = max(50, args.steps // 4)
-        on_ms, _ = ist.timed(n_i, args.warmup, with_check=True)
-        off_ms, _ = ist.timed(n_i, args.warmup, with_check=False)
-        # the check kernel alone
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for _ in range(5):
-            ist.check()
-        ev0.record()
-        for _ in range(n_i):
-            ist.check()
-        ev1.record()
-        torch.cuda.synchronize()
-        chk_us = 1e3 * ev0.elapsed_time(ev1) / n_i
+        n_i = max(50, args.steps // 2)
+        on_ms = max_over_ranks(ist.timed_graph(n_i, args.warmup, with_check=True))
+        off_ms = max_over_ranks(ist.timed_graph(n_i, args.warmup, with_check=False))
+        reps = 20
+        chk_ms = max_over_ranks(ist.timed_graph(n_i // 10 + 1, 3, checks_only=reps))
+        chk_us = 1e3 * chk_ms / ((n_i // 10 + 1) * reps)
+        clean_aborts = int(ist.mask.sum().item())
+        del ist, idb
+        torch.cuda.empty_cache()
+        # the workload as specified: 1% of in-use pages reallocated (stale)
+        sdb = W.device_batch(iw, device, seed=iw.seed + rank)
+        sst = Step(sdb, "fp8", device)
+        st_ms = max_over_ranks(sst.timed_graph(n_i, args.warmup, with_check=True))
         line["integrity_check"] = {
-            "workload": workload_text(iw, idb), "aborted_requests": int(ist.mask.sum().item()),
+            "workload": workload_text(iw, sdb),
+            "overhead_variant": "same shape, 0%% stale pages (%d aborted)" % clean_aborts,
             "step_ms_with_check": on_ms / n_i, "step_ms_without_check": off_ms / n_i,
             "overhead_pct": 100.0 * (on_ms - off_ms) / off_ms, "check_kernel_us": chk_us,
-            "check_share_of_step_pct": 100.0 * chk_us / (1e3 * on_ms / n_i)}
-        del ist, idb
+            "check_share_of_step_pct": 100.0 * chk_us / (1e3 * on_ms / n_i),
+            "stale_1pct": {"aborted_requests": int(sst.mask.sum().item()), "step_ms": st_ms / n_i},
+            "timing": "CUDA-graph-captured steps"}
+        del sst, sdb
         torch.cuda.empty_cache()
 
     derr = fkv.device_error()

@@ -40,15 +40,17 @@ def _headers():
     return hs + [os.path.join(ROOT, "include", "fkv.h")]
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_lib: str = LIB,
+          build_dir: str = BUILD_DIR) -> str:
+    """Compile every source (only what changed) and link ``out_lib``."""
+    os.makedirs(build_dir, exist_ok=True)
     exe = nvcc()
     hdrs = _headers()
     jobs = []
     objs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s, *hdrs]):
             jobs.append([exe, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", s, "-o", o])
@@ -62,11 +64,11 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + ".tmp%d" % os.getpid()
+    if force or jobs or _stale(out_lib, objs):
+        tmp = out_lib + ".tmp%d" % os.getpid()
         run([exe, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, out_lib)
+    return out_lib
 
 
 if __name__ == "__main__":

@@ -10,24 +10,27 @@
 // convert values as it reads them; requests aborted by the separate integrity
 // check are not read (fail closed).
 //
-// GB300 design (three launches, chained with programmatic dependent launch):
+// GB300 design (two launches, chained with programmatic dependent launch):
 //  1. plan (one CTA): tiles per request from seq_lens / abort mask / page
-//     table; prefix over requests; the first request of each worker warp.
-//     A "tile" is 32 tokens of one (request, KV head) unit.
+//     table; prefix over requests; the first request of each worker warp;
+//     zeroed arrival counters.  A "tile" is kTile tokens of one
+//     (request, KV head) unit.
 //  2. attention (persistent, one warp per CTA, grid = SMs x resident CTAs):
 //     the concatenation of all units' tiles is cut into equal contiguous
-//     ranges, one per warp (split-KV with perfect balance across the lognormal
+//     ranges, one per warp (split-KV with even load across the lognormal
 //     context mix).  Each warp streams its tiles through a private ring of
 //     shared-memory stages filled by 128B-swizzled TMA tensor copies (one 2-D
-//     box per page: K and V tiles of a (page, head) are contiguous in HBM).
+//     box per page: the K and V tiles of a (page, head) are contiguous in HBM).
 //     QK^T and PV run on the tensor cores as m16n8k16 MMAs with tokens on M
 //     and the G <= 8 query heads of the KV head on N; e4m3 codes become f16
 //     exactly in registers (the per-head scales fold into the logit factor and
 //     the output); softmax is online in fp32 with warp shuffles.  A warp that
 //     covers a whole unit writes the bf16 output directly; otherwise it writes
-//     an unnormalised fp32 partial (o, m, l) to the workspace.
-//  3. combine: merges the partials of each split unit (log-sum-exp rescale),
-//     zero-fills aborted / empty / invalid rows.
+//     an unnormalised fp32 partial (o, m, l), and the last of the unit's warps
+//     to arrive (an atomic counter, no waiting) merges the partials with a
+//     log-sum-exp rescale (two levels for units split over many warps).  Rows
+//     of requests with no tiles (aborted, empty, malformed) are zero-filled by
+//     the warps, one request each.
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -35,16 +38,58 @@
 
 #include "fkv_common.cuh"
 
+// Tokens per pipeline stage and ring depth of each KV dtype.
+#ifndef FKV_FP8_TILE
+#define FKV_FP8_TILE 64
+#endif
+#ifndef FKV_FP8_STAGES
+#define FKV_FP8_STAGES 3
+#endif
+#ifndef FKV_BF16_TILE
+#define FKV_BF16_TILE 64
+#endif
+#ifndef FKV_BF16_STAGES
+#define FKV_BF16_STAGES 2
+#endif
+
 namespace fkv {
 
 constexpr int kD = 128;
-constexpr int kTileT = 32;               // tokens per pipeline stage
 constexpr int kMaxGroup = 8;             // query heads sharing a KV head (MMA N)
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanSmemPrefix = 4096;    // requests whose prefix the plan searches in smem
-constexpr int kCombineWarps = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // a copy that has not landed in 2 s has failed
 constexpr uint64_t kDrainLimitNs = 200000000ull;
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr int kChunk = 6;                // parts merged per first-level merge of a long unit
+
+template <bool kFp8>
+struct Cfg;
+template <>
+struct Cfg<true> {
+    static constexpr int kTile = FKV_FP8_TILE;
+    static constexpr int kStages = FKV_FP8_STAGES;
+    static constexpr int kHalves = 1;           // 128-byte-wide column blocks per token row
+};
+template <>
+struct Cfg<false> {
+    static constexpr int kTile = FKV_BF16_TILE;
+    static constexpr int kStages = FKV_BF16_STAGES;
+    static constexpr int kHalves = 2;
+};
+
+template <bool kFp8>
+struct Layout {
+    static constexpr int kTile = Cfg<kFp8>::kTile;
+    static constexpr int kStages = Cfg<kFp8>::kStages;
+    static constexpr int kHalves = Cfg<kFp8>::kHalves;
+    static constexpr int kHalfBytes = kTile * 128;              // one column block of a K (or V) tile
+    static constexpr int kTileBytes = kHalves * kHalfBytes;     // a K (or V) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;          // K then V
+    static constexpr int kSmem = 1024 + kStages * kStageBytes + 8 * kStages;
+    static_assert(kTile == 32 || kTile == 64, "tile of 32 or 64 tokens");
+    static_assert(kHalfBytes % 1024 == 0, "stage buffers stay 1024-byte aligned for the 128B swizzle");
+};
 
 struct AttnParams {
     const __nv_bfloat16 *q;
@@ -53,48 +98,32 @@ struct AttnParams {
     const int32_t *indptr;
     const int32_t *indices;
     const int32_t *seq_lens;
-    const uint8_t *abort_mask;
     const int64_t *prefix;     // [B+1] tile prefix over requests (tiles x Hkv)
     const int32_t *warp_req;   // [NW] request holding each warp's first tile
-    float *part_o;             // [slots][G][D]
+    float *part_o;             // [slots][G][D]   slots = B*Hkv + NW
     float2 *part_ml;           // [slots][G]  (m in log2 units, l; l < 0 marks an invalid unit)
+    int32_t *counters;         // [B*Hkv] arrivals per split unit (or per chunk of it)
+    int32_t *chunk_counters;   // [slots] arrivals per first-level chunk, indexed by its first slot
     __nv_bfloat16 *out;
     uint32_t *err;
     int B, Hq, Hkv, G, P, S, NW;
     float sm_scale_log2;
 };
 
-template <bool kFp8>
-struct KvTraits;
-template <>
-struct KvTraits<true> {
-    static constexpr int kStages = 3;
-    static constexpr int kTileBytes = kTileT * kD;       // one K (or V) stage tile
-};
-template <>
-struct KvTraits<false> {
-    static constexpr int kStages = 3;
-    static constexpr int kTileBytes = kTileT * kD * 2;   // two 128-byte-wide halves
-};
-constexpr int kHalfBytes = kTileT * 128;
-
-template <bool kFp8>
-constexpr int attn_smem_bytes() {
-    return 1024 + KvTraits<kFp8>::kStages * 2 * KvTraits<kFp8>::kTileBytes + 64;
-}
-
 // ---------------------------------------------------------------------------
 // 1. plan
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kPlanThreads)
 attn_plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ indptr,
-                 const uint8_t *__restrict__ abort_mask, int64_t nnz, int B, int Hkv, int S, int NW,
-                 int64_t *__restrict__ prefix, int32_t *__restrict__ warp_req) {
-    // let the attention grid start its prologue now
-    grid_dep_launch();
+                 const uint8_t *__restrict__ abort_mask, int64_t nnz, int B, int Hkv, int S, int tile, int NW,
+                 int64_t *__restrict__ prefix, int32_t *__restrict__ warp_req, int32_t *__restrict__ counters) {
+    grid_dep_wait();                   // the abort mask of the integrity check is complete
+    grid_dep_launch();                 // let the attention grid start its prologue
     __shared__ int64_t s_warp_tot[kPlanThreads / 32];
     __shared__ int64_t s_prefix[kPlanSmemPrefix + 1];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    // arrival counters: one per unit, then one per partial slot (chunks)
+    for (int64_t u = tid; u < 2 * static_cast<int64_t>(B) * Hkv + NW; u += kPlanThreads) counters[u] = 0;
     int64_t carry = 0;
     for (int base = 0; base < B; base += kPlanThreads) {
         const int r = base + tid;
@@ -104,12 +133,12 @@ attn_plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict
             const int64_t b = indptr[r], e = indptr[r + 1];
             const bool alive = abort_mask == nullptr || abort_mask[r] == 0;
             if (alive && sl > 0 && b >= 0 && e >= b && e <= nnz && (e - b) * S >= sl)
-                cnt = ((sl + kTileT - 1) / kTileT) * Hkv;
+                cnt = ((sl + tile - 1) / tile) * Hkv;
         }
         int64_t x = cnt;                                   // inclusive warp scan
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+            const int64_t y = __shfl_up_sync(kFull, x, o);
             if (lane >= o) x += y;
         }
         if (lane == 31) s_warp_tot[wid] = x;
@@ -118,7 +147,7 @@ attn_plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict
             int64_t v = s_warp_tot[lane];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int64_t y = __shfl_up_sync(0xffffffffu, v, o);
+                const int64_t y = __shfl_up_sync(kFull, v, o);
                 if (lane >= o) v += y;
             }
             s_warp_tot[lane] = v;                           // inclusive over warps
@@ -143,7 +172,6 @@ attn_plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict
         const int64_t lo = static_cast<int64_t>(w) * T / NW;
         int res = B;
         if (lo < T) {
-            // largest r with prefix[r] <= lo (then prefix[r+1] > lo since lo < T)
             int a = 0, z = B;                              // invariant: prefix[a] <= lo < prefix[z]
             while (z - a > 1) {
                 const int mid = (a + z) >> 1;
@@ -157,7 +185,7 @@ attn_plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict
 }
 
 // ---------------------------------------------------------------------------
-// 2. split attention
+// 2. split attention with fused merge
 // ---------------------------------------------------------------------------
 struct Cursor {
     int r, h, tt, nt;
@@ -188,19 +216,113 @@ __device__ __forceinline__ void cursor_next(Cursor &c, const AttnParams &p) {
 __device__ __forceinline__ uint32_t lo16(uint32_t x) { return x & 0xFFFFu; }
 __device__ __forceinline__ uint32_t hi16(uint32_t x) { return x >> 16; }
 
+// first tile of warp w's range
+__device__ __forceinline__ int64_t warp_lo(int64_t w, int64_t T, int NW) { return w * T / NW; }
+
+// the warp w with floor(w*T/NW) <= x < floor((w+1)*T/NW)
+__device__ __forceinline__ int64_t warp_of_tile(int64_t x, int64_t T, int NW) {
+    const int64_t w = ((x + 1) * NW + T - 1) / T - 1;
+    return w < NW - 1 ? w : NW - 1;
+}
+
+// Merge n partials stored at slots slot0, slot0 + stride, ... into either the
+// final bf16 rows of unit (r, h) (scaled by vsc / L) or one fp32 partial
+// written to slot `dst` (the first level of a two-level merge).  With
+// `maybe_empty` (tiles < warps) entries of warps with an empty range, which
+// wrote nothing, are skipped; entry j belongs to warp wk0 + j.
+//
+// Lanes cover (entry, head) pairs for the softmax statistics (lane = k*8 + hd,
+// four entries per pass), so every head's max and sum come from one round of
+// loads and shuffles; the output pass keeps the loads of all heads of an entry
+// in flight together (lane = 4 output dims).
+__device__ void merge_parts(const AttnParams &p, int64_t slot0, int n, int stride, bool maybe_empty, int64_t wk0,
+                            int64_t T, bool final_out, int r, int h, float vsc, int64_t dst) {
+    const int lane = threadIdx.x;
+    const int G = p.G;
+    auto empty = [&](int j) {
+        return maybe_empty && warp_lo(wk0 + j, T, p.NW) == warp_lo(wk0 + j + 1, T, p.NW);
+    };
+    const int hd_l = lane & 7, k_l = lane >> 3;
+    // pass 1: per-head max and invalid flag
+    float mmax = -INFINITY;
+    bool bad = false;
+    for (int k0 = 0; k0 < n; k0 += 4) {
+        const int k = k0 + k_l;
+        if (hd_l < G && k < n && !empty(k)) {
+            const float2 ml = __ldcg(p.part_ml + (slot0 + static_cast<int64_t>(k) * stride) * G + hd_l);
+            bad |= ml.y < 0.f;
+            mmax = fmaxf(mmax, ml.x);
+        }
+    }
+    mmax = fmaxf(mmax, __shfl_xor_sync(kFull, mmax, 8));
+    mmax = fmaxf(mmax, __shfl_xor_sync(kFull, mmax, 16));
+    bad = __any_sync(kFull, bad);
+    // pass 2: per-head normaliser
+    float ltot = 0.f;
+    for (int k0 = 0; k0 < n; k0 += 4) {
+        const int k = k0 + k_l;
+        if (hd_l < G && k < n && !empty(k)) {
+            const float2 ml = __ldcg(p.part_ml + (slot0 + static_cast<int64_t>(k) * stride) * G + hd_l);
+            ltot += ex2(ml.x - mmax) * ml.y;
+        }
+    }
+    ltot += __shfl_xor_sync(kFull, ltot, 8);
+    ltot += __shfl_xor_sync(kFull, ltot, 16);
+    // pass 3: weighted sum of the partial outputs, 4 dims per lane, all heads at once
+    float4 acc[kMaxGroup];
+#pragma unroll
+    for (int hd = 0; hd < kMaxGroup; ++hd) acc[hd] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!bad) {
+        for (int k = 0; k < n; ++k) {
+            if (empty(k)) continue;
+            const int64_t slot = slot0 + static_cast<int64_t>(k) * stride;
+            float2 mlv = make_float2(-INFINITY, 0.f);
+            if (lane < G) mlv = __ldcg(p.part_ml + slot * G + lane);
+#pragma unroll
+            for (int hd = 0; hd < kMaxGroup; ++hd) {
+                if (hd >= G) break;
+                const float f = ex2(__shfl_sync(kFull, mlv.x, hd) - __shfl_sync(kFull, mmax, hd));
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (slot * G + hd) * kD) + lane);
+                acc[hd].x += f * v.x;
+                acc[hd].y += f * v.y;
+                acc[hd].z += f * v.z;
+                acc[hd].w += f * v.w;
+            }
+        }
+    }
+    if (final_out) {
+#pragma unroll
+        for (int hd = 0; hd < kMaxGroup; ++hd) {
+            if (hd >= G) break;
+            const float sc = bad ? 0.f : vsc / __shfl_sync(kFull, ltot, hd);
+            uint2 *orow =
+                reinterpret_cast<uint2 *>(p.out + (static_cast<int64_t>(r) * p.Hq + h * G + hd) * kD) + lane;
+            *orow = make_uint2(pack_bf16x2(acc[hd].x * sc, acc[hd].y * sc),
+                               pack_bf16x2(acc[hd].z * sc, acc[hd].w * sc));
+        }
+    } else {
+#pragma unroll
+        for (int hd = 0; hd < kMaxGroup; ++hd) {
+            if (hd >= G) break;
+            __stcg(reinterpret_cast<float4 *>(p.part_o + (dst * G + hd) * kD) + lane, acc[hd]);
+        }
+        if (lane < G) __stcg(p.part_ml + dst * G + lane, make_float2(mmax, bad ? -1.f : ltot));
+    }
+}
+
 template <bool kFp8>
 __global__ void __launch_bounds__(32, 1)
 paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV) {
-    using Tr = KvTraits<kFp8>;
-    constexpr int NST = Tr::kStages;
-    constexpr int kTileBytes = Tr::kTileBytes;
-    constexpr int kStageBytes = 2 * kTileBytes;
-    constexpr uint32_t FULL = 0xffffffffu;
+    using Lay = Layout<kFp8>;
+    constexpr int kTile = Lay::kTile;
+    constexpr int NST = Lay::kStages;
+    constexpr int MT = kTile / 16;                       // 16-token MMA tiles per stage
+    constexpr int NACC = MT >= 4 ? 1 : 2;                // independent QK accumulator chains per M tile
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t bars = sbase + NST * kStageBytes;
+    const uint32_t bars = sbase + NST * Lay::kStageBytes;
     const int lane = threadIdx.x;
     const int g = lane >> 2, t = lane & 3;
     const int w = blockIdx.x;
@@ -216,8 +338,14 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     grid_dep_wait();                                   // plan results are visible
 
     const int64_t T = p.prefix[p.B];
-    const int64_t lo = static_cast<int64_t>(w) * T / p.NW;
-    const int64_t hi = static_cast<int64_t>(w + 1) * T / p.NW;
+    // rows of requests with no tiles (aborted, empty, malformed) are zero
+    for (int r = w; r < p.B; r += p.NW) {
+        if (p.prefix[r + 1] != p.prefix[r]) continue;
+        uint4 *orow = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(r) * p.Hq * kD);
+        for (int c = lane; c < p.Hq * kD / 8; c += 32) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    const int64_t lo = warp_lo(w, T, p.NW);
+    const int64_t hi = warp_lo(w + 1, T, p.NW);
     if (lo >= hi) {
         grid_dep_launch();
         return;
@@ -246,7 +374,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             pbase += 32;
             pidB = fetch_ids(pbase + 32);
         }
-        return __shfl_sync(FULL, pidA, pos - pbase);
+        return __shfl_sync(kFull, pidA, pos - pbase);
     };
     auto issue = [&](int stage) {
         if (L.r != pid_r) {
@@ -256,42 +384,38 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             lneed = (lseq + S - 1) / S;
             pbase = -1000;
         }
-        const int tok0 = L.tt * kTileT;
-        const int npg = S < kTileT ? kTileT / S : 1;
-        const int rows = S < kTileT ? S : kTileT;
+        const int tok0 = L.tt * kTile;
+        const int npg = S < kTile ? kTile / S : 1;       // pages per tile (<= 4)
+        const int rows = S < kTile ? S : kTile;
         const int pos0 = tok0 / S;
-        const int rowoff = S < kTileT ? 0 : tok0 % S;
-        int ids[2] = {-1, -1};
+        const int rowoff = S < kTile ? 0 : tok0 % S;
+        int ids[4] = {-1, -1, -1, -1};
         bool bad = false;
         uint32_t bytes = 0;
-        for (int k = 0; k < npg; ++k) {
-            const int pos = pos0 + k;
-            if (pos >= lneed) break;                   // page beyond the request's last token
-            int id = page_id(pos);
-            if (id < 0 || id >= p.P) {                 // never dereference an id outside the pool
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (k >= npg || pos0 + k >= lneed) break;    // page beyond the request's last token
+            int id = page_id(pos0 + k);
+            if (id < 0 || id >= p.P) {                   // never dereference an id outside the pool
                 bad = true;
                 id = 0;
             }
             ids[k] = id;
-            bytes += 2u * rows * (kFp8 ? kD : 2 * kD);
+            bytes += 2u * rows * 128u * Lay::kHalves;
         }
         bad_bits = (bad_bits & ~(1u << stage)) | (static_cast<uint32_t>(bad) << stage);
         if (lane == 0) {
             const uint32_t bar = bars + 8 * stage;
             mbar_arrive_expect_tx(bar, bytes);
-            for (int k = 0; k < npg; ++k) {
-                if (ids[k] < 0) continue;
-                const uint32_t dk = sbase + stage * kStageBytes + k * rows * 128;
-                const uint32_t dv = dk + kTileBytes;
-                if (kFp8) {
-                    tma_load_4d(dk, &tmK, bar, 0, rowoff, L.h, ids[k], policy);
-                    tma_load_4d(dv, &tmV, bar, 0, rowoff, L.h, ids[k], policy);
-                } else {
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        tma_load_4d(dk + half * kHalfBytes, &tmK, bar, half * 64, rowoff, L.h, ids[k], policy);
-                        tma_load_4d(dv + half * kHalfBytes, &tmV, bar, half * 64, rowoff, L.h, ids[k], policy);
-                    }
+            for (int k = 0; k < 4; ++k) {
+                if (ids[k] < 0) break;
+                const uint32_t dk = sbase + stage * Lay::kStageBytes + k * rows * 128;
+                const uint32_t dv = dk + Lay::kTileBytes;
+#pragma unroll
+                for (int half = 0; half < Lay::kHalves; ++half) {
+                    tma_load_4d(dk + half * Lay::kHalfBytes, &tmK, bar, half * 64, rowoff, L.h, ids[k], policy);
+                    tma_load_4d(dv + half * Lay::kHalfBytes, &tmV, bar, half * 64, rowoff, L.h, ids[k], policy);
                 }
             }
         }
@@ -353,8 +477,8 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                     amax = fmaxf(amax, fabsf(__uint_as_float(qw[j] << 16)));
                     amax = fmaxf(amax, fabsf(__uint_as_float(qw[j] & 0xFFFF0000u)));
                 }
-                amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 2));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
                 int e = amax > 0.f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127 : 0;
                 e = max(-100, min(127, e));
                 const float sc = __uint_as_float(static_cast<uint32_t>(127 + 14 - e) << 23);
@@ -367,7 +491,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                 const float ksc = __ldg(p.k_scale + C.h) * p.sm_scale_log2;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    const int ej = __shfl_sync(FULL, e, (2 * t + j) * 4);
+                    const int ej = __shfl_sync(kFull, e, (2 * t + j) * 4);
                     cfac[j] = ksc * __uint_as_float(static_cast<uint32_t>(127 + ej - 14) << 23);
                 }
             } else {
@@ -394,27 +518,29 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             if (!unit_bad && lane == 0) atomicOr(p.err, FKV_DEVERR_ATTN_PAGE);
             unit_bad = true;
         }
-        const uint32_t kbase = sbase + s * kStageBytes;
-        const uint32_t vbase = kbase + kTileBytes;
-        const int nvalid = min(kTileT, cseq - C.tt * kTileT);
+        const uint32_t kbase = sbase + s * Lay::kStageBytes;
+        const uint32_t vbase = kbase + Lay::kTileBytes;
+        const int nvalid = min(kTile, cseq - C.tt * kTile);
 
-        if (nvalid < kTileT) {
+        if (nvalid < kTile) {
             // rows past the request's last token hold stale bytes: zero V there
             // (K rows are masked out of the softmax instead)
-            const int nch = (kTileT - nvalid) * 8;
+            const int nch = (kTile - nvalid) * 8;
 #pragma unroll
-            for (int half = 0; half < (kFp8 ? 1 : 2); ++half)
+            for (int half = 0; half < Lay::kHalves; ++half)
                 for (int c = lane; c < nch; c += 32)
-                    st_shared_v4_zero(vbase + half * kHalfBytes + nvalid * 128 + c * 16);
+                    st_shared_v4_zero(vbase + half * Lay::kHalfBytes + nvalid * 128 + c * 16);
             fence_proxy_async_smem();
             __syncwarp();
         }
 
-        // ---- S^T = K Q^T : tokens on M (two 16-row tiles), heads on N ----
-        float sacc[2][4];
+        // ---- S^T = K Q^T : tokens on M (16-row tiles), heads on N ----
+        float sacc[MT][4];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
+        for (int mt = 0; mt < MT; ++mt) {
+            float acc[NACC][4];
+#pragma unroll
+            for (int a = 0; a < NACC; ++a) acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
             const int ra = mt * 16 + g, rb = ra + 8;
             if (kFp8) {
                 // this lane's 32 dims of rows ra, rb: 16-byte chunks 2t, 2t+1 (swizzled)
@@ -426,7 +552,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                 const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    mma_f16(sacc[mt], e4m3x2_to_f16x2(lo16(wa[ks])), e4m3x2_to_f16x2(lo16(wb[ks])),
+                    mma_f16(acc[ks % NACC], e4m3x2_to_f16x2(lo16(wa[ks])), e4m3x2_to_f16x2(lo16(wb[ks])),
                             e4m3x2_to_f16x2(hi16(wa[ks])), e4m3x2_to_f16x2(hi16(wb[ks])), qb[ks][0], qb[ks][1]);
                 }
             } else {
@@ -435,31 +561,37 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int half = k >> 1, c = 2 * t + (k & 1);
-                    const uint4 va = ld_shared_v4(kbase + half * kHalfBytes + ra * 128 + ((c ^ (ra & 7)) << 4));
-                    const uint4 vb = ld_shared_v4(kbase + half * kHalfBytes + rb * 128 + ((c ^ (rb & 7)) << 4));
+                    const uint4 va = ld_shared_v4(kbase + half * Lay::kHalfBytes + ra * 128 + ((c ^ (ra & 7)) << 4));
+                    const uint4 vb = ld_shared_v4(kbase + half * Lay::kHalfBytes + rb * 128 + ((c ^ (rb & 7)) << 4));
                     wa[4 * k] = va.x; wa[4 * k + 1] = va.y; wa[4 * k + 2] = va.z; wa[4 * k + 3] = va.w;
                     wb[4 * k] = vb.x; wb[4 * k + 1] = vb.y; wb[4 * k + 2] = vb.z; wb[4 * k + 3] = vb.w;
                 }
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16(sacc[mt], wa[2 * ks], wb[2 * ks], wa[2 * ks + 1], wb[2 * ks + 1], qb[ks][0], qb[ks][1]);
+                    mma_bf16(acc[ks % NACC], wa[2 * ks], wb[2 * ks], wa[2 * ks + 1], wb[2 * ks + 1], qb[ks][0],
+                             qb[ks][1]);
             }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sacc[mt][c] = NACC == 2 ? acc[0][c] + acc[NACC - 1][c] : acc[0][c];
         }
 
         // ---- online softmax (log2 domain); columns are heads 2t, 2t+1 ----
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < MT; ++mt) {
             if (mt * 16 + g >= nvalid) sacc[mt][0] = sacc[mt][1] = -INFINITY;
             if (mt * 16 + g + 8 >= nvalid) sacc[mt][2] = sacc[mt][3] = -INFINITY;
         }
-        float mx[2];
-        mx[0] = fmaxf(fmaxf(sacc[0][0], sacc[0][2]), fmaxf(sacc[1][0], sacc[1][2]));
-        mx[1] = fmaxf(fmaxf(sacc[0][1], sacc[0][3]), fmaxf(sacc[1][1], sacc[1][3]));
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            mx[0] = fmaxf(mx[0], fmaxf(sacc[mt][0], sacc[mt][2]));
+            mx[1] = fmaxf(mx[1], fmaxf(sacc[mt][1], sacc[mt][3]));
+        }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            mx[j] = fmaxf(mx[j], __shfl_xor_sync(FULL, mx[j], 4));
-            mx[j] = fmaxf(mx[j], __shfl_xor_sync(FULL, mx[j], 8));
-            mx[j] = fmaxf(mx[j], __shfl_xor_sync(FULL, mx[j], 16));
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(kFull, mx[j], 4));
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(kFull, mx[j], 8));
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(kFull, mx[j], 16));
         }
         float alpha[2];
 #pragma unroll
@@ -468,13 +600,17 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             alpha[j] = ex2(m[j] - mnew);
             m[j] = mnew;
         }
-        float pr[2][4];
+        float pr[MT][4];
+        float ls[2] = {0.f, 0.f};
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) pr[mt][c] = ex2(fmaf(sacc[mt][c], cfac[c & 1], -m[c & 1]));
-        l[0] = l[0] * alpha[0] + ((pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]));
-        l[1] = l[1] * alpha[1] + ((pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
+            for (int c = 0; c < 4; ++c) {
+                pr[mt][c] = ex2(fmaf(sacc[mt][c], cfac[c & 1], -m[c & 1]));
+                ls[c & 1] += pr[mt][c];
+            }
+        l[0] = l[0] * alpha[0] + ls[0];
+        l[1] = l[1] * alpha[1] + ls[1];
 #pragma unroll
         for (int a = 0; a < 8; ++a) {
             o[a][0] *= alpha[0];
@@ -486,9 +622,9 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
         // FP8: P in f16 (11-bit significand).  BF16: the MMA needs bf16 P, whose
         // 8-bit significand alone would cost up to 2^-9 |v| in the output, so P
         // is split into bf16 hi + lo parts and PV runs on both (16 bits).
-        uint32_t pb[2][2], pl[2][2];
+        uint32_t pb[MT][2], pl[MT][2];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < MT; ++mt) {
             if (kFp8) {
                 pb[mt][0] = movmatrix_trans(pack_f16x2(pr[mt][0], pr[mt][1]));
                 pb[mt][1] = movmatrix_trans(pack_f16x2(pr[mt][2], pr[mt][3]));
@@ -509,7 +645,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
 
         // ---- O^T += V^T P^T : dims on M (8 blocks of 16), tokens on K ----
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < MT; ++mt) {
             const int r0 = mt * 16 + 2 * t, r1 = r0 + 1, r2 = r0 + 8, r3 = r0 + 9;
             if (kFp8) {
                 // dims 16g .. 16g+15 of four token rows (16-byte chunk g, swizzled)
@@ -534,7 +670,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                 uint32_t a[8], b[8], c[8], d[8];
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    const uint32_t hb = vbase + half * kHalfBytes;
+                    const uint32_t hb = vbase + half * Lay::kHalfBytes;
                     const uint4 A = ld_shared_v4(hb + r0 * 128 + ((g ^ (r0 & 7)) << 4));
                     const uint4 Bv = ld_shared_v4(hb + r1 * 128 + ((g ^ (r1 & 7)) << 4));
                     const uint4 Cv = ld_shared_v4(hb + r2 * 128 + ((g ^ (r2 & 7)) << 4));
@@ -566,12 +702,12 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             float lt[2] = {l[0], l[1]};
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                lt[j] += __shfl_xor_sync(FULL, lt[j], 4);
-                lt[j] += __shfl_xor_sync(FULL, lt[j], 8);
-                lt[j] += __shfl_xor_sync(FULL, lt[j], 16);
+                lt[j] += __shfl_xor_sync(kFull, lt[j], 4);
+                lt[j] += __shfl_xor_sync(kFull, lt[j], 8);
+                lt[j] += __shfl_xor_sync(kFull, lt[j], 16);
             }
             const bool whole = seg_start == 0 && C.tt == C.nt - 1;
-            const int u = C.r * Hkv + C.h;
+            const int64_t u = static_cast<int64_t>(C.r) * Hkv + C.h;
             const float vsc = kFp8 ? __ldg(p.v_scale + C.h) : 1.f;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
@@ -601,79 +737,62 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                     *reinterpret_cast<uint4 *>(orow + d0) = r0v;
                     *reinterpret_cast<uint4 *>(orow + d1) = r1v;
                 } else {
-                    const int64_t slot = static_cast<int64_t>(u) + w;
+                    const int64_t slot = u + w;
                     float *prow = p.part_o + (slot * G + hd) * kD;
-                    *reinterpret_cast<float4 *>(prow + d0) = make_float4(v[0], v[1], v[2], v[3]);
-                    *reinterpret_cast<float4 *>(prow + d0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
-                    *reinterpret_cast<float4 *>(prow + d1) = make_float4(v[8], v[9], v[10], v[11]);
-                    *reinterpret_cast<float4 *>(prow + d1 + 4) = make_float4(v[12], v[13], v[14], v[15]);
-                    if (g == 0) p.part_ml[slot * G + hd] = make_float2(m[j], unit_bad ? -1.f : lt[j]);
+                    __stcg(reinterpret_cast<float4 *>(prow + d0), make_float4(v[0], v[1], v[2], v[3]));
+                    __stcg(reinterpret_cast<float4 *>(prow + d0 + 4), make_float4(v[4], v[5], v[6], v[7]));
+                    __stcg(reinterpret_cast<float4 *>(prow + d1), make_float4(v[8], v[9], v[10], v[11]));
+                    __stcg(reinterpret_cast<float4 *>(prow + d1 + 4), make_float4(v[12], v[13], v[14], v[15]));
+                    if (g == 0) __stcg(p.part_ml + slot * G + hd, make_float2(m[j], unit_bad ? -1.f : lt[j]));
+                }
+            }
+            if (!whole) {
+                // Merge without waiting: the last of the unit's warps to arrive
+                // merges.  Units split over more than kChunk warps merge in two
+                // levels (chunks of kChunk consecutive parts, then the chunks),
+                // so no single warp reads a long unit's partials serially.
+                const int64_t s0 = p.prefix[C.r] + static_cast<int64_t>(C.h) * C.nt;
+                const int64_t wf = warp_of_tile(s0, T, p.NW), wl = warp_of_tile(s0 + C.nt - 1, T, p.NW);
+                const int span = static_cast<int>(wl - wf + 1);
+                const bool maybe_empty = T < p.NW;
+                __threadfence();
+                __syncwarp();
+                if (maybe_empty || span <= kChunk) {
+                    int nparts = span;
+                    if (maybe_empty) {
+                        nparts = 0;
+                        for (int64_t x = wf; x <= wl; ++x) nparts += warp_lo(x, T, p.NW) != warp_lo(x + 1, T, p.NW);
+                    }
+                    int last = 0;
+                    if (lane == 0) last = atomicAdd(p.counters + u, 1) == nparts - 1;
+                    if (__shfl_sync(kFull, last, 0)) {
+                        __threadfence();
+                        merge_parts(p, u + wf, span, 1, maybe_empty, wf, T, true, C.r, C.h, vsc, 0);
+                    }
+                } else {
+                    const int c0 = (static_cast<int>(w - wf) / kChunk) * kChunk;
+                    const int csz = min(kChunk, span - c0);
+                    const int nch = (span + kChunk - 1) / kChunk;
+                    int last = 0;
+                    if (lane == 0) last = atomicAdd(p.chunk_counters + (u + wf + c0), 1) == csz - 1;
+                    if (__shfl_sync(kFull, last, 0)) {
+                        __threadfence();
+                        merge_parts(p, u + wf + c0, csz, 1, false, wf + c0, T, false, C.r, C.h, vsc, u + wf + c0);
+                        __threadfence();
+                        __syncwarp();
+                        int last2 = 0;
+                        if (lane == 0) last2 = atomicAdd(p.counters + u, 1) == nch - 1;
+                        if (__shfl_sync(kFull, last2, 0)) {
+                            __threadfence();
+                            merge_parts(p, u + wf, nch, kChunk, false, wf, T, true, C.r, C.h, vsc, 0);
+                        }
+                    }
                 }
             }
         }
         cursor_next(C, p);
     }
     grid_dep_launch();
-}
-
-// ---------------------------------------------------------------------------
-// 3. combine split units
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ int64_t warp_of_tile(int64_t x, int64_t T, int NW) {
-    // the warp w with floor(w*T/NW) <= x < floor((w+1)*T/NW)
-    const int64_t w = ((x + 1) * NW + T - 1) / T - 1;
-    return w < NW - 1 ? w : NW - 1;
-}
-
-__global__ void __launch_bounds__(32 * kCombineWarps)
-attn_combine_kernel(const AttnParams p, int kv_fp8) {
-    grid_dep_wait();                                  // partials are visible
-    const int lane = threadIdx.x & 31;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
-    if (row >= static_cast<int64_t>(p.B) * p.Hq) return;
-    const int r = static_cast<int>(row / p.Hq);
-    const int i = static_cast<int>(row % p.Hq);
-    const int h = i / p.G, hd = i % p.G;
-    uint2 *orow = reinterpret_cast<uint2 *>(p.out + row * kD) + lane;   // 4 bf16 per lane
-    const int64_t T = p.prefix[p.B];
-    const int64_t ntr = (p.prefix[r + 1] - p.prefix[r]) / p.Hkv;
-    if (ntr == 0) {                                   // aborted, empty or malformed: zero row
-        *orow = make_uint2(0u, 0u);
-        return;
-    }
-    const int64_t s0 = p.prefix[r] + h * ntr;
-    const int64_t wf = warp_of_tile(s0, T, p.NW), wl = warp_of_tile(s0 + ntr - 1, T, p.NW);
-    if (wf == wl) return;                             // one warp covered it and wrote it
-    const int64_t u = static_cast<int64_t>(r) * p.Hkv + h;
-    // warps with an empty range (possible when tiles < warps) wrote no partial
-    auto empty = [&](int64_t w) { return w * T / p.NW == (w + 1) * T / p.NW; };
-    float mmax = -INFINITY;
-    bool bad = false;
-    for (int64_t w = wf; w <= wl; ++w) {
-        if (empty(w)) continue;
-        const float2 ml = p.part_ml[(u + w) * p.G + hd];
-        bad |= ml.y < 0.f;
-        mmax = fmaxf(mmax, ml.x);
-    }
-    if (bad) {
-        *orow = make_uint2(0u, 0u);
-        return;
-    }
-    float ltot = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t w = wf; w <= wl; ++w) {
-        if (empty(w)) continue;
-        const float2 ml = p.part_ml[(u + w) * p.G + hd];
-        const float f = ex2(ml.x - mmax);
-        ltot += f * ml.y;
-        const float4 v = reinterpret_cast<const float4 *>(p.part_o + ((u + w) * p.G + hd) * kD)[lane];
-        acc.x += f * v.x;
-        acc.y += f * v.y;
-        acc.z += f * v.z;
-        acc.w += f * v.w;
-    }
-    const float sc = (kv_fp8 ? __ldg(p.v_scale + h) : 1.f) / ltot;
-    *orow = make_uint2(pack_bf16x2(acc.x * sc, acc.y * sc), pack_bf16x2(acc.z * sc, acc.w * sc));
 }
 
 // ---------------------------------------------------------------------------
@@ -706,7 +825,7 @@ int ctas_per_sm() {
     std::lock_guard<std::mutex> lk(g_mu);
     int &v = g_ctas_per_sm[dev][kFp8 ? 1 : 0];
     if (!v) {
-        const int smem = attn_smem_bytes<kFp8>();
+        const int smem = Layout<kFp8>::kSmem;
         if (cudaFuncSetAttribute(paged_decode_attn_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem) != cudaSuccess)
             return 0;
@@ -729,21 +848,23 @@ int grid_warps(bool fp8) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-    size_t prefix, warp_req, part_ml, part_o, total;
+    size_t prefix, warp_req, counters, part_ml, part_o, total;
 };
 
 WsLayout ws_layout(int B, int Hkv, int G, int NW) {
     WsLayout L;
-    const size_t slots = static_cast<size_t>(B) * Hkv + NW;
+    const size_t units = static_cast<size_t>(B) * Hkv;
+    const size_t slots = units + NW;
     L.prefix = 0;
     L.warp_req = align256(L.prefix + sizeof(int64_t) * (static_cast<size_t>(B) + 1));
-    L.part_ml = align256(L.warp_req + sizeof(int32_t) * NW);
+    L.counters = align256(L.warp_req + sizeof(int32_t) * NW);
+    L.part_ml = align256(L.counters + sizeof(int32_t) * (units + slots));
     L.part_o = align256(L.part_ml + sizeof(float2) * slots * G);
     L.total = align256(L.part_o + sizeof(float) * slots * G * kD);
     return L;
 }
 
-bool make_kv_map(CUtensorMap *m, const void *base, bool fp8, int P, int Hkv, int S) {
+bool make_kv_map(CUtensorMap *m, const void *base, bool fp8, int P, int Hkv, int S, int tile) {
     auto enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t es = fp8 ? 1 : 2;
@@ -751,28 +872,13 @@ bool make_kv_map(CUtensorMap *m, const void *base, bool fp8, int P, int Hkv, int
                                 static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(P)};
     const cuuint64_t strides[3] = {kD * es, static_cast<cuuint64_t>(S) * kD * es,
                                    static_cast<cuuint64_t>(Hkv) * S * kD * es};
-    const cuuint32_t box[4] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(S < kTileT ? S : kTileT), 1u, 1u};
+    const cuuint32_t box[4] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(S < tile ? S : tile), 1u, 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     const CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                            const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
-}
-
-template <typename Kern, typename... Args>
-cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 }  // namespace
@@ -819,10 +925,11 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
     if (NW <= 0 || !err) return FKV_ERR_CUDA;
     const WsLayout wl = ws_layout(batch, num_kv_heads, G, NW);
     if (workspace_bytes < wl.total) return FKV_ERR_INVALID_ARG;
+    const int tile = fp8 ? Layout<true>::kTile : Layout<false>::kTile;
 
     CUtensorMap tmK, tmV;
-    if (!make_kv_map(&tmK, k_cache, fp8, num_pages, num_kv_heads, page_size) ||
-        !make_kv_map(&tmV, v_cache, fp8, num_pages, num_kv_heads, page_size))
+    if (!make_kv_map(&tmK, k_cache, fp8, num_pages, num_kv_heads, page_size, tile) ||
+        !make_kv_map(&tmV, v_cache, fp8, num_pages, num_kv_heads, page_size, tile))
         return FKV_ERR_CUDA;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -833,9 +940,10 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
     p.indptr = page_indptr;
     p.indices = page_indices;
     p.seq_lens = seq_lens;
-    p.abort_mask = abort_mask;
     p.prefix = reinterpret_cast<const int64_t *>(ws + wl.prefix);
     p.warp_req = reinterpret_cast<const int32_t *>(ws + wl.warp_req);
+    p.counters = reinterpret_cast<int32_t *>(ws + wl.counters);
+    p.chunk_counters = p.counters + static_cast<int64_t>(batch) * num_kv_heads;
     p.part_ml = reinterpret_cast<float2 *>(ws + wl.part_ml);
     p.part_o = reinterpret_cast<float *>(ws + wl.part_o);
     p.out = static_cast<__nv_bfloat16 *>(out);
@@ -850,20 +958,15 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
     p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    attn_plan_kernel<<<1, kPlanThreads, 0, st>>>(seq_lens, page_indptr, abort_mask, nnz, batch, num_kv_heads,
-                                                   page_size, NW, reinterpret_cast<int64_t *>(ws + wl.prefix),
-                                                   reinterpret_cast<int32_t *>(ws + wl.warp_req));
-    FKV_CHECK_LAUNCH();
-    cudaError_t e;
-    if (fp8)
-        e = launch_pdl(paged_decode_attn_kernel<true>, dim3(NW), dim3(32), attn_smem_bytes<true>(), st, p, tmK, tmV);
-    else
-        e = launch_pdl(paged_decode_attn_kernel<false>, dim3(NW), dim3(32), attn_smem_bytes<false>(), st, p, tmK,
-                       tmV);
+    cudaError_t e = launch_pdl(attn_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, seq_lens, page_indptr,
+                               abort_mask, nnz, batch, num_kv_heads, page_size, tile, NW,
+                               reinterpret_cast<int64_t *>(ws + wl.prefix), reinterpret_cast<int32_t *>(ws + wl.warp_req),
+                               reinterpret_cast<int32_t *>(ws + wl.counters));
     if (e != cudaSuccess) return FKV_ERR_CUDA;
-    const int64_t rows = static_cast<int64_t>(batch) * num_q_heads;
-    const unsigned cblocks = static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps);
-    e = launch_pdl(attn_combine_kernel, dim3(cblocks), dim3(32 * kCombineWarps), 0, st, p, fp8 ? 1 : 0);
+    if (fp8)
+        e = launch_pdl(paged_decode_attn_kernel<true>, dim3(NW), dim3(32), Layout<true>::kSmem, st, p, tmK, tmV);
+    else
+        e = launch_pdl(paged_decode_attn_kernel<false>, dim3(NW), dim3(32), Layout<false>::kSmem, st, p, tmK, tmV);
     if (e != cudaSuccess) return FKV_ERR_CUDA;
     return FKV_OK;
 }

@@ -78,6 +78,6 @@ extern "C" int32_t fkv_kernels_per_call(const char *entry_point) {
     if (!entry_point) return -1;
     const std::string e(entry_point);
     if (e == "kv_append_fp8" || e == "kv_append_bf16" || e == "kv_page_tag_check") return 1;
-    if (e == "paged_decode_attn") return 3;   // plan, split attention, combine
+    if (e == "paged_decode_attn") return 2;   // plan, split attention with fused merge
     return -1;
 }

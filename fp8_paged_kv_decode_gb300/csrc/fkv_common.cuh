@@ -26,6 +26,25 @@ bool aligned16(const void *p);
         if (cudaGetLastError() != cudaSuccess) return FKV_ERR_CUDA; \
     } while (0)
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream finishes; it must call grid_dep_wait()
+// before touching anything that kernel produces (every kernel here does so
+// first thing), which also keeps completion ordered transitively.
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ---------------------------------------------------------------------------
 // device helpers
 // ---------------------------------------------------------------------------

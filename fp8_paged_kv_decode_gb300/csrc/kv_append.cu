@@ -25,6 +25,8 @@ kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ 
                      const float *__restrict__ k_scale, const float *__restrict__ v_scale,
                      uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
                      int32_t num_pages, int32_t num_kv_heads, int32_t page_size, uint32_t *err) {
+    grid_dep_wait();        // earlier readers of the pool (attention) have finished
+    grid_dep_launch();
     const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t per_token = static_cast<int64_t>(num_kv_heads) * 2 * kChunks;
     const int64_t n = gid / per_token;
@@ -70,6 +72,8 @@ kv_append_bf16_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__
                       const int64_t *__restrict__ slots, int64_t n_tokens,
                       uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                       int32_t num_pages, int32_t num_kv_heads, int32_t page_size, uint32_t *err) {
+    grid_dep_wait();        // earlier readers of the pool (attention) have finished
+    grid_dep_launch();
     const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t per_token = static_cast<int64_t>(num_kv_heads) * 2 * kChunks;
     const int64_t n = gid / per_token;
@@ -122,11 +126,11 @@ extern "C" fkv_status kv_append_fp8(const void *k_new, const void *v_new, const 
     const int64_t threads = static_cast<int64_t>(n_tokens) * num_kv_heads * 2 * kChunks;
     const int64_t blocks = (threads + 255) / 256;
     if (blocks > 0x7FFFFFFFLL) return FKV_ERR_INVALID_ARG;
-    kv_append_fp8_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping, n_tokens,
-        k_scale, v_scale, k_cache, v_cache, num_pages, num_kv_heads, page_size, err);
-    FKV_CHECK_LAUNCH();
-    return FKV_OK;
+    const cudaError_t e = launch_pdl(kv_append_fp8_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                                     static_cast<cudaStream_t>(stream), static_cast<const uint4 *>(k_new),
+                                     static_cast<const uint4 *>(v_new), slot_mapping, static_cast<int64_t>(n_tokens),
+                                     k_scale, v_scale, k_cache, v_cache, num_pages, num_kv_heads, page_size, err);
+    return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
 }
 
 extern "C" fkv_status kv_append_bf16(const void *k_new, const void *v_new, const int64_t *slot_mapping,
@@ -141,9 +145,10 @@ extern "C" fkv_status kv_append_bf16(const void *k_new, const void *v_new, const
     const int64_t threads = static_cast<int64_t>(n_tokens) * num_kv_heads * 2 * kChunks;
     const int64_t blocks = (threads + 255) / 256;
     if (blocks > 0x7FFFFFFFLL) return FKV_ERR_INVALID_ARG;
-    kv_append_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping, n_tokens,
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_pages, num_kv_heads, page_size, err);
-    FKV_CHECK_LAUNCH();
-    return FKV_OK;
+    const cudaError_t e = launch_pdl(kv_append_bf16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                                     static_cast<cudaStream_t>(stream), static_cast<const uint4 *>(k_new),
+                                     static_cast<const uint4 *>(v_new), slot_mapping, static_cast<int64_t>(n_tokens),
+                                     static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_pages,
+                                     num_kv_heads, page_size, err);
+    return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
 }

@@ -24,6 +24,8 @@ kv_page_tag_check_kernel(const uint32_t *__restrict__ page_tags, int32_t num_pag
                          const int32_t *__restrict__ page_indptr, const int32_t *__restrict__ page_indices,
                          const uint32_t *__restrict__ expected_tags, int64_t nnz,
                          uint8_t *__restrict__ abort_mask) {
+    grid_dep_wait();        // tags and tables written by earlier kernels are visible
+    grid_dep_launch();
     const int r = blockIdx.x;
     const int64_t begin = __ldg(page_indptr + r);
     const int64_t end = __ldg(page_indptr + r + 1);
@@ -71,8 +73,8 @@ extern "C" fkv_status kv_page_tag_check(const uint32_t *page_tags, int32_t num_p
     if (!page_indptr || !abort_mask) return FKV_ERR_INVALID_ARG;
     if (nnz > 0 && (!page_indices || !expected_tags)) return FKV_ERR_INVALID_ARG;
     if (num_pages > 0 && !page_tags) return FKV_ERR_INVALID_ARG;
-    kv_page_tag_check_kernel<<<batch, kCheckThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        page_tags, num_pages, page_indptr, page_indices, expected_tags, nnz, abort_mask);
-    FKV_CHECK_LAUNCH();
-    return FKV_OK;
+    const cudaError_t e = launch_pdl(kv_page_tag_check_kernel, dim3(batch), dim3(kCheckThreads), 0,
+                                     static_cast<cudaStream_t>(stream), page_tags, num_pages, page_indptr,
+                                     page_indices, expected_tags, nnz, abort_mask);
+    return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
 }

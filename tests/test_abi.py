@@ -42,7 +42,7 @@ def test_library_loads_in_tree(lib_path):
     for s in declared_symbols():
         assert hasattr(lib, s)
     assert lib.fkv_status_string(0) == b"ok"
-    assert fkv.kernels_per_call("paged_decode_attn") == 3
+    assert fkv.kernels_per_call("paged_decode_attn") == 2
     assert fkv.kernels_per_call("kv_page_tag_check") == 1
 
 
