@@ -38,7 +38,7 @@ if ROOT not in sys.path:
 METRIC = "decode attn tokens/s & HBM GB/s (% of 8 TB/s) at 64 req, FP8 vs BF16 KV"
 HEADLINE = "pages_shaped_64req"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--kv", default="fp8", choices=["fp8", "bf16"], help="KV cache dtype of the main line")
     ap.add_argument("--skip-extras", action="store_true", help="only the FP8 headline and e2e")
     ap.add_argument("--cpu-requests", type=int, default=4, help="requests in the oracle's bounded sample")
     return ap.parse_args()
@@ -85,11 +86,15 @@ def recorded_traffic(kv):
     """DRAM bytes per paged_decode_attn call from a committed ncu summary, if it
     was taken on the current kernel source (else None)."""
     try:
+        vals = {}
         with open(TRAFFIC_FILE) as f:
-            t = json.load(f)
-        e = t.get(kv)
-        if e and e.get("source_hash") == kernel_source_hash():
-            return e
+            for line in f:
+                line = line.strip()
+                if line and not line.startswith("#") and "=" in line:
+                    k, v = line.split("=", 1)
+                    vals[k.strip()] = v.strip()
+        if vals.get(kv + ".source_hash") == kernel_source_hash():
+            return {"dram_bytes_per_call": int(vals[kv + ".dram_bytes_per_call"])}
     except Exception:
         pass
     return None
@@ -450,7 +455,7 @@ def main():
 
     wl = W.WORKLOADS[args.workload]
     db = W.device_batch(wl, device, seed=wl.seed + rank)
-    fp8 = Step(db, "fp8", device)
+    fp8 = Step(db, args.kv, device)
     fkv.device_error(clear=True)
     sampler = ClockSampler(local)
     total_ms, attn_ms = fp8.timed(args.steps, args.warmup, sampler=sampler)
@@ -461,7 +466,7 @@ def main():
     attn_bytes, attended = fp8.attn_bytes()
     peak, peak_kind = peak_hbm()
     achieved = attn_bytes / (attn_ms / 1e3) / 1e9
-    traffic = recorded_traffic("fp8")
+    traffic = recorded_traffic(args.kv)
 
     e2e_steps = max(10, args.steps // 4)
     e2e_ms, bi, bo = fp8.timed_e2e(e2e_steps, max(3, args.warmup // 4))
@@ -471,12 +476,14 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3 KV -> f16 MMA, f32 accumulate", "data": "synthetic",
-        "config": {"workload": workload_text(wl, db), "kv_dtype": "fp8_e4m3", "global_batch": world * wl.batch,
-                   "step": "kv_append_fp8 + kv_page_tag_check + paged_decode_attn (one layer)",
+        "vs_baseline": None, "dtype": "e4m3 KV -> f16 MMA, f32 accumulate" if args.kv == "fp8" else
+        "bf16 KV -> bf16 MMA, f32 accumulate", "data": "synthetic",
+        "config": {"workload": workload_text(wl, db), "kv_dtype": "fp8_e4m3" if args.kv == "fp8" else "bf16",
+                   "global_batch": world * wl.batch,
+                   "step": "kv_append_%s + kv_page_tag_check + paged_decode_attn (one layer)" % args.kv,
                    "l2": "inputs larger than L2 (%.2f GB of KV read per step); no flush" % (attn_bytes / 1e9),
                    "parallelism": "replicas x%d" % world},
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_attn (plan + split attention + combine)",
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_attn (plan + split attention with fused merge)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "traffic": traffic["dram_bytes_per_call"] if traffic else None,
                      "algorithmic_bytes": attn_bytes, "attn_ms": attn_ms,
@@ -489,7 +496,7 @@ def main():
         "clocks": sampler.summary(),
     }
 
-    if not args.skip_extras:
+    if not args.skip_extras and args.kv == "fp8":
         bf = Step(db, "bf16", device)
         bms, battn = bf.timed(max(10, args.steps // 2), args.warmup)
         bms, battn = max_over_ranks(bms), max_over_ranks(battn)
@@ -538,7 +545,7 @@ def main():
         line["device_error"] = derr
     if rank == 0:
         t0 = time.perf_counter()
-        s, n, text = oracle_sample(db, "fp8", args.cpu_requests)
+        s, n, text = oracle_sample(db, args.kv, args.cpu_requests)
         line["cpu_baseline"] = {"value": n / s, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": text}
         print(json.dumps(line), flush=True)
     if _PG is not None:
