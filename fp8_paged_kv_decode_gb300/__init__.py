@@ -21,6 +21,7 @@ import threading
 __all__ = [
     "FkvError", "KV_FP8_E4M3", "KV_BF16", "library_path", "load_library", "kv_append_fp8", "kv_append_bf16",
     "kv_page_tag_check", "paged_decode_attn", "paged_decode_attn_workspace_size", "alloc_workspace",
+    "paged_decode_attn_noalloc",
     "device_error", "kernels_per_call", "EXPORTED_SYMBOLS",
 ]
 
@@ -33,8 +34,11 @@ HEAD_DIM = 128
 
 EXPORTED_SYMBOLS = (
     "fkv_status_string", "kv_append_fp8", "kv_append_bf16", "kv_page_tag_check",
-    "paged_decode_attn_workspace_size", "paged_decode_attn", "fkv_device_error", "fkv_kernels_per_call",
+    "paged_decode_attn_workspace_size", "paged_decode_attn", "paged_decode_attn_noalloc", "fkv_device_error",
+    "fkv_kernels_per_call",
 )
+ERR_SCRATCH_LIMIT = 4
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -73,6 +77,9 @@ def load_library():
         lib.paged_decode_attn.restype = ctypes.c_int
         lib.paged_decode_attn.argtypes = [P, i32, i32, P, P, i32, P, P, i32, i32, i32, i32, P, P, i64, P, P, f32,
                                           P, P, ctypes.c_size_t, P]
+        lib.paged_decode_attn_noalloc.restype = ctypes.c_int
+        lib.paged_decode_attn_noalloc.argtypes = [P, i32, i32, P, P, i32, P, P, i32, i32, i32, i32, P, P, i64, P, P,
+                                                  f32, P, P]
         lib.fkv_device_error.restype = ctypes.c_int
         lib.fkv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         lib.fkv_kernels_per_call.restype = i32
@@ -202,6 +209,31 @@ def paged_decode_attn(q, k_cache, v_cache, page_indptr, page_indices, seq_lens, 
         float(sm_scale),
         _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
         "paged_decode_attn")
+    return out
+
+
+def paged_decode_attn_noalloc(q, k_cache, v_cache, page_indptr, page_indices, seq_lens, sm_scale, out,
+                              k_scale=None, v_scale=None, abort_mask=None, stream=None):
+    """``paged_decode_attn`` without a workspace argument, for callers that
+    cannot allocate device memory: its scratch is a fixed array of
+    ``NOALLOC_SCRATCH_BYTES`` inside the library (shared by all calls on a
+    device, so calls must not overlap on the GPU).  Shapes needing more
+    scratch raise FkvError (status ERR_SCRATCH_LIMIT)."""
+    import torch
+    _dev(q, k_cache, v_cache, page_indptr, page_indices, seq_lens, out, k_scale, v_scale, abort_mask)
+    fp8 = _is_byte_cache(k_cache)
+    _need(fp8 or k_cache.dtype == torch.bfloat16, "cache must be uint8 (e4m3) or bf16")
+    _need(q.dtype == torch.bfloat16 and out.dtype == torch.bfloat16, "q/out must be bf16")
+    _need(seq_lens.dtype == torch.int32, "seq_lens must be int32")
+    _need(abort_mask is None or abort_mask.dtype == torch.uint8, "abort_mask must be uint8")
+    B, Hq, D = q.shape
+    P, Hkv, S, D2 = k_cache.shape
+    _need(tuple(out.shape) == (B, Hq, D) and D2 == D and page_indptr.numel() == B + 1, "shape mismatch")
+    _raise(load_library().paged_decode_attn_noalloc(
+        _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), KV_FP8_E4M3 if fp8 else KV_BF16,
+        _ptr(k_scale) if fp8 else None, _ptr(v_scale) if fp8 else None, P, Hkv, S, D,
+        _ptr(page_indptr), _ptr(page_indices), page_indices.numel(), _ptr(seq_lens), _ptr(abort_mask),
+        float(sm_scale), _ptr(out), _stream(stream)), "paged_decode_attn_noalloc")
     return out
 
 

@@ -57,6 +57,7 @@ extern "C" const char *fkv_status_string(fkv_status s) {
         case FKV_ERR_INVALID_ARG: return "invalid argument";
         case FKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
         case FKV_ERR_CUDA: return "CUDA runtime error";
+        case FKV_ERR_SCRATCH_LIMIT: return "shape needs more scratch than the no-allocation entry point holds";
     }
     return "unknown status";
 }
@@ -78,6 +79,6 @@ extern "C" int32_t fkv_kernels_per_call(const char *entry_point) {
     if (!entry_point) return -1;
     const std::string e(entry_point);
     if (e == "kv_append_fp8" || e == "kv_append_bf16" || e == "kv_page_tag_check") return 1;
-    if (e == "paged_decode_attn") return 2;   // plan, split attention with fused merge
+    if (e == "paged_decode_attn" || e == "paged_decode_attn_noalloc") return 2;   // plan, split attention
     return -1;
 }

@@ -59,7 +59,9 @@ typedef enum {
     FKV_OK = 0,
     FKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment, small workspace */
     FKV_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim != 128, group > 8, ...) */
-    FKV_ERR_CUDA = 3           /* a CUDA runtime call or launch failed */
+    FKV_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    FKV_ERR_SCRATCH_LIMIT = 4  /* paged_decode_attn_noalloc: the shape needs more scratch than
+                                  FKV_NOALLOC_SCRATCH_BYTES */
 } fkv_status;
 
 typedef enum {
@@ -182,6 +184,48 @@ FKV_API fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t num_q
                              int64_t nnz, const int32_t *seq_lens, const uint8_t *abort_mask,
                              float sm_scale, void *out,
                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * paged_decode_attn_noalloc -- paged_decode_attn for callers that cannot
+ * allocate device memory.  (The pages describe no such entry point; it has no
+ * counterpart there.)
+ *
+ * Who needs it: code that has no allocator of its own -- a plugin inside a
+ * host runtime that owns all device memory and passes the plugin only its
+ * input and output buffers -- and serving loops that forbid cudaMalloc on the
+ * hot path because it can synchronise the device and stall other streams.
+ * Neither can hand paged_decode_attn its workspace.
+ *
+ * What it does: exactly paged_decode_attn (same arguments, same results,
+ * same fail-closed rules) minus the workspace arguments.  Its scratch is one
+ * fixed device array of FKV_NOALLOC_SCRATCH_BYTES compiled into the library;
+ * every GPU that loads the library reserves that array until the process
+ * exits.  The call itself allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library routine).
+ *
+ * Limits and rules:
+ *   - A shape whose workspace (paged_decode_attn_workspace_size) exceeds
+ *     FKV_NOALLOC_SCRATCH_BYTES is rejected with FKV_ERR_SCRATCH_LIMIT before
+ *     anything is launched.  With 8 query heads per KV head, 16 MiB covers
+ *     roughly batch * num_kv_heads up to 3000 on a 152-SM GB300.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array and it keeps whatever the
+ *     last call left in it (each call clears what it needs cleared).  Calls
+ *     that overlap on the GPU -- on different streams, or from different host
+ *     threads without ordering -- race on it and give wrong results; order
+ *     them on one stream or serialise them.
+ */
+#define FKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+FKV_API fkv_status paged_decode_attn_noalloc(const void *q, int32_t batch, int32_t num_q_heads,
+                                     const void *k_cache, const void *v_cache, int32_t kv_dtype,
+                                     const float *k_scale, const float *v_scale,
+                                     int32_t num_pages, int32_t num_kv_heads,
+                                     int32_t page_size, int32_t head_dim,
+                                     const int32_t *page_indptr, const int32_t *page_indices,
+                                     int64_t nnz, const int32_t *seq_lens, const uint8_t *abort_mask,
+                                     float sm_scale, void *out, void *stream);
 
 /*
  * fkv_device_error -- read (and optionally clear) the sticky device error word
