@@ -287,6 +287,39 @@ class Step:
         barrier()
         return t0.elapsed_time(t1)
 
+    def time_realloc(self, frac, reps):
+        """kv_page_realloc of a seeded ``frac`` of the in-use pages, with and
+        without the scrub of their K and V bytes (CUDA-graph timed)."""
+        torch, fkv = self.torch, self.fkv
+        rng = np.random.default_rng(7)
+        ind = self.db.pt.indices
+        moved = np.sort(rng.choice(ind, size=max(1, round(frac * ind.size)), replace=False)).astype(np.int32)
+        pages = torch.from_numpy(moved).to(self.device)
+        new = torch.zeros(moved.size, dtype=torch.int32, device=self.device)
+        res = {"pages": int(moved.size)}
+        for name, kc, vc in (("tags_only", None, None), ("with_scrub", self.k_cache, self.v_cache)):
+            fkv.kv_page_realloc(self.page_tags, pages, new, kc, vc)
+            torch.cuda.synchronize(self.device)
+            s = torch.cuda.Stream(self.device)
+            s.wait_stream(torch.cuda.current_stream(self.device))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(10):
+                    fkv.kv_page_realloc(self.page_tags, pages, new, kc, vc)
+            g.replay()
+            torch.cuda.synchronize(self.device)
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for _ in range(reps):
+                g.replay()
+            t1.record()
+            torch.cuda.synchronize(self.device)
+            us = 1e3 * t0.elapsed_time(t1) / (10 * reps)
+            res[name + "_us"] = us
+        page_bytes = 2 * self.Hkv * self.S * self.D * (1 if self.fp8 else 2)
+        res["scrub_gbs"] = moved.size * page_bytes / (res["with_scrub_us"] * 1e3)
+        return res
+
     def timed_e2e(self, steps, warmup):
         """The same step through host buffers: every step copies its inputs from
         pinned host memory and reads the output and abort mask back."""
@@ -403,29 +436,54 @@ def workload_text(wl, db):
 
 
 def run_reference(args):
-    """Reference arm: the CPU oracle as it stands, one bounded sample per step."""
+    """Reference arm: the CPU oracle as it stands.  Each step is one query-head
+    row of one request (its new token appended, its pages checked, that row
+    attended), cycling over all heads of the first few requests; the
+    requests' cached context is encoded by the oracle before timing."""
     world, rank, local = dist_env()
     if rank != 0:
         return
     import torch
+    import oracle
     from fp8_paged_kv_decode_gb300 import workloads as W
+    orc = oracle.default()
     wl = W.WORKLOADS[args.workload]
     device = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
     db = W.device_batch(wl, device, seed=wl.seed)
-    times = []
+    n_req = min(4, wl.batch)
+    cr = W.compact_requests(db, list(range(n_req)))
+    S, Hkv, D, Hq = wl.page_size, wl.num_kv_heads, wl.head_dim, wl.num_q_heads
+    kc = np.zeros((cr.num_pages, Hkv, S, D), np.uint8)
+    vc = np.zeros((cr.num_pages, Hkv, S, D), np.uint8)
+    new_idx = np.cumsum(cr.seq_lens.astype(np.int64)) - 1
+    ctx_sel = np.ones(cr.slots.size, bool)
+    ctx_sel[new_idx] = False
+    orc.kv_append_fp8(cr.k_tokens[ctx_sel], cr.v_tokens[ctx_sel], cr.slots[ctx_sel], db.k_scale, db.v_scale, kc, vc)
+    tags = db.pt.page_tags[cr.orig_pages]
+    exp = np.concatenate([db.pt.expected_tags[db.pt.indptr[r]:db.pt.indptr[r + 1]] for r in range(n_req)])
+    sm = 1.0 / np.sqrt(D)
+    total = 0.0
     for i in range(args.warmup + args.steps):
-        s, n, text = oracle_sample(db, "fp8", 1, start=i)
+        j = (i // Hq) % n_req
+        row = j * Hq + i % Hq
+        t0 = time.perf_counter()
+        orc.kv_append_fp8(cr.k_tokens[new_idx[j]:new_idx[j] + 1], cr.v_tokens[new_idx[j]:new_idx[j] + 1],
+                          cr.slots[new_idx[j]:new_idx[j] + 1], db.k_scale, db.v_scale, kc, vc)
+        mask = orc.kv_page_tag_check(tags, cr.indptr, cr.indices, exp)
+        orc.paged_decode_attn(cr.q, kc, vc, cr.indptr, cr.indices, cr.seq_lens, sm, k_scale=db.k_scale,
+                              v_scale=db.v_scale, abort_mask=mask, rows=[row])
         if i >= args.warmup:
-            times.append(s)
-    total = float(np.sum(times))
-    value = args.steps / total
+            total += time.perf_counter() - t0
+    value = (args.steps / Hq) / total          # decode tokens/s: Hq rows make one request's token
+    sample = ("one query-head row per step (cycling over the %d heads of the first %d requests, %d context "
+              "tokens), with that request's append and tag check; 1 thread" % (Hq, n_req, int(cr.seq_lens.sum())))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_text(wl, db), "step": "one request per step: append+check+attention"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": "one request of the batch per step (cycling), all query heads, 1 thread"},
+        "config": {"workload": workload_text(wl, db), "kv_dtype": "fp8_e4m3",
+                   "step": "CPU oracle: append + tag check + attention, one query-head row"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -504,7 +562,8 @@ def main():
         bach = bbytes / (battn / 1e3) / 1e9
         line["bf16_kv"] = {"value": world * wl.batch * max(10, args.steps // 2) / (bms / 1e3), "unit": "tokens/s",
                            "ms_per_step": bms / max(10, args.steps // 2), "attn_ms": battn, "attn_gbs": bach,
-                           "frac": bach / peak, "algorithmic_bytes": bbytes}
+                           "frac": bach / peak, "algorithmic_bytes": bbytes,
+                           "traffic": (recorded_traffic("bf16") or {}).get("dram_bytes_per_call")}
         line["fp8_over_bf16_attn_time"] = battn / attn_ms
         del bf
         torch.cuda.empty_cache()
@@ -529,6 +588,7 @@ def main():
         sdb = W.device_batch(iw, device, seed=iw.seed + rank)
         sst = Step(sdb, "fp8", device)
         st_ms = max_over_ranks(sst.timed_graph(n_i, args.warmup, with_check=True))
+        realloc = sst.time_realloc(frac=0.01, reps=max(20, n_i // 10))
         line["integrity_check"] = {
             "workload": workload_text(iw, sdb),
             "overhead_variant": "same shape, 0%% stale pages (%d aborted)" % clean_aborts,
@@ -536,6 +596,7 @@ def main():
             "overhead_pct": 100.0 * (on_ms - off_ms) / off_ms, "check_kernel_us": chk_us,
             "check_share_of_step_pct": 100.0 * chk_us / (1e3 * on_ms / n_i),
             "stale_1pct": {"aborted_requests": int(sst.mask.sum().item()), "step_ms": st_ms / n_i},
+            "device_realloc_1pct": realloc,
             "timing": "CUDA-graph-captured steps"}
         del sst, sdb
         torch.cuda.empty_cache()

@@ -9,6 +9,7 @@ the library is missing or no GPU is present the calls raise.
 Entry points (same names as the C ABI):
   kv_append_fp8 / kv_append_bf16   write new tokens into the paged pools
   kv_page_tag_check                the separate per-page generation-tag check
+  kv_page_realloc                  bump tags (and optionally zero pages) of reallocated pages
   paged_decode_attn                decode attention over the paged cache
   paged_decode_attn_workspace_size bytes of scratch paged_decode_attn needs
 """
@@ -20,7 +21,8 @@ import threading
 
 __all__ = [
     "FkvError", "KV_FP8_E4M3", "KV_BF16", "library_path", "load_library", "kv_append_fp8", "kv_append_bf16",
-    "kv_page_tag_check", "paged_decode_attn", "paged_decode_attn_workspace_size", "alloc_workspace",
+    "kv_page_tag_check", "kv_page_realloc", "paged_decode_attn", "paged_decode_attn_workspace_size",
+    "alloc_workspace",
     "paged_decode_attn_noalloc",
     "device_error", "kernels_per_call", "EXPORTED_SYMBOLS",
 ]
@@ -30,10 +32,11 @@ KV_BF16 = 1
 DEVERR_APPEND_SLOT = 0x1
 DEVERR_ATTN_PAGE = 0x2
 DEVERR_TIMEOUT = 0x4
+DEVERR_REALLOC_PAGE = 0x8
 HEAD_DIM = 128
 
 EXPORTED_SYMBOLS = (
-    "fkv_status_string", "kv_append_fp8", "kv_append_bf16", "kv_page_tag_check",
+    "fkv_status_string", "kv_append_fp8", "kv_append_bf16", "kv_page_tag_check", "kv_page_realloc",
     "paged_decode_attn_workspace_size", "paged_decode_attn", "paged_decode_attn_noalloc", "fkv_device_error",
     "fkv_kernels_per_call",
 )
@@ -72,6 +75,8 @@ def load_library():
         lib.kv_append_bf16.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, P]
         lib.kv_page_tag_check.restype = ctypes.c_int
         lib.kv_page_tag_check.argtypes = [P, i32, P, P, P, i32, i64, P, P]
+        lib.kv_page_realloc.restype = ctypes.c_int
+        lib.kv_page_realloc.argtypes = [P, i32, P, i32, P, P, P, i32, i32, i32, i32, P]
         lib.paged_decode_attn_workspace_size.restype = ctypes.c_size_t
         lib.paged_decode_attn_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.paged_decode_attn.restype = ctypes.c_int
@@ -171,6 +176,25 @@ def kv_page_tag_check(page_tags, page_indptr, page_indices, expected_tags, abort
     _raise(load_library().kv_page_tag_check(_ptr(page_tags), page_tags.numel(), _ptr(page_indptr),
                                             _ptr(page_indices), _ptr(expected_tags), B, page_indices.numel(),
                                             _ptr(abort_mask), _stream(stream)), "kv_page_tag_check")
+
+
+def kv_page_realloc(page_tags, pages, new_tags, k_cache=None, v_cache=None, stream=None):
+    """Bump the live tag of each listed page (new owners record ``new_tags``)
+    and, if the pools are given, zero those pages."""
+    import torch
+    _dev(page_tags, pages, new_tags, k_cache, v_cache)
+    _need(page_tags.dtype in (torch.int32, torch.uint32) and new_tags.dtype == page_tags.dtype, "32-bit tags")
+    _need(pages.dtype == torch.int32 and new_tags.numel() == pages.numel(), "pages int32, one new tag each")
+    if k_cache is not None:
+        _need(v_cache is not None and tuple(k_cache.shape) == tuple(v_cache.shape), "both pools, same shape")
+        P, Hkv, S, D = k_cache.shape
+        kv = KV_FP8_E4M3 if _is_byte_cache(k_cache) else KV_BF16
+    else:
+        Hkv = S = 0
+        D, kv = HEAD_DIM, KV_FP8_E4M3
+    _raise(load_library().kv_page_realloc(_ptr(page_tags), page_tags.numel(), _ptr(pages), pages.numel(),
+                                          _ptr(new_tags), _ptr(k_cache), _ptr(v_cache), kv, Hkv, S, D,
+                                          _stream(stream)), "kv_page_realloc")
 
 
 def paged_decode_attn_workspace_size(batch, num_q_heads, num_kv_heads, head_dim=HEAD_DIM, kv_dtype=KV_FP8_E4M3):

@@ -73,6 +73,7 @@ typedef enum {
 #define FKV_DEVERR_APPEND_SLOT   0x1u  /* kv_append_*: slot beyond the pool, token skipped */
 #define FKV_DEVERR_ATTN_PAGE     0x2u  /* paged_decode_attn: page id outside [0, num_pages), row zeroed */
 #define FKV_DEVERR_TIMEOUT       0x4u  /* a bounded wait on a copy gave up; the call's output is not valid */
+#define FKV_DEVERR_REALLOC_PAGE  0x8u  /* kv_page_realloc: a listed id is outside [0, num_pages), skipped */
 
 FKV_API const char *fkv_status_string(fkv_status s);
 
@@ -136,6 +137,33 @@ FKV_API fkv_status kv_page_tag_check(const uint32_t *page_tags, int32_t num_page
                              const int32_t *page_indptr, const int32_t *page_indices,
                              const uint32_t *expected_tags, int32_t batch, int64_t nnz,
                              uint8_t *abort_mask, void *stream);
+
+/*
+ * kv_page_realloc -- hand pages to new owners on the device ("Kimi and GLM
+ * Reasoning Slimming: Hands-On Test", section "Giving Every Physical Cache
+ * Page a 'Generation Number'": a page's tag changes each time it is
+ * reallocated, so holders of the old (page, tag) pair fail the check; the
+ * same page names clearing GPU memory as a further defence).  For each j:
+ *     p = pages[j]; page_tags[p] += 1 (modulo 2^32); new_tags[j] = page_tags[p]
+ * and, when k_cache / v_cache are given, every byte of page p in both pools
+ * is zeroed (all KV heads).  new_tags[j] is the tag the new owner records as
+ * its expected tag.
+ *
+ *   page_tags   uint32 [num_pages], updated in place
+ *   pages       int32 [n]; list each page at most once per call (a repeated
+ *               page still ends with its tag bumped once per listing, but
+ *               which listing receives which new tag is unspecified)
+ *   new_tags    uint32 [n] output; 0 for an id outside [0, num_pages), which
+ *               is skipped and sets FKV_DEVERR_REALLOC_PAGE
+ *   k_cache, v_cache  both NULL (no scrub) or the pools of this layer, of
+ *               dtype kv_dtype with num_kv_heads, page_size, head_dim = 128
+ * n == 0 is a no-op.
+ */
+FKV_API fkv_status kv_page_realloc(uint32_t *page_tags, int32_t num_pages,
+                                   const int32_t *pages, int32_t n, uint32_t *new_tags,
+                                   void *k_cache, void *v_cache, int32_t kv_dtype,
+                                   int32_t num_kv_heads, int32_t page_size, int32_t head_dim,
+                                   void *stream);
 
 /*
  * paged_decode_attn_workspace_size -- bytes of device workspace that

@@ -16,6 +16,9 @@ Parity status of each function (what pins it independently of itself is in
   against a hand-computed position, untouched bytes.
 * ``kv_page_tag_check`` -- pinned: hand-derived cases in ``tests/golden``,
   brute force, tag bump and 32-bit wrap-around.
+* ``kv_page_realloc`` -- pinned: reallocation then the (pinned) tag check
+  aborts exactly the old holders; a fresh holder of the new tag passes;
+  wrap-around; scrub zeroes exactly the listed pages.
 * ``paged_decode_attn`` -- pinned: single-token context returns V, identical
   keys give the mean of V, numpy dense softmax on tiny inputs, G=1 per-head
   softmax, page-permutation invariance, FP8-vs-BF16 on exactly representable
@@ -89,6 +92,8 @@ class Oracle:
         lib.oracle_paged_decode_attn.argtypes = [
             P, i32, i32, P, P, i32, P, P, i32, i32, i32, i32,
             P, P, i64, P, P, ctypes.c_double, P, i32, P]
+        lib.oracle_kv_page_realloc.restype = None
+        lib.oracle_kv_page_realloc.argtypes = [P, i32, P, i32, P, P, P, i32, i32, i32, i32]
         self.lib = lib
         self.path = path
 
@@ -149,6 +154,23 @@ class Oracle:
         self.lib.oracle_kv_page_tag_check(_ptr(tags), P, _ptr(indptr), _ptr(indices),
                                           _ptr(exp), B, int(indices.size), _ptr(out))
         return out
+
+    def kv_page_realloc(self, page_tags, pages, k_cache=None, v_cache=None):
+        """In place: bump the live tag of every listed page (uint32, wraps) and,
+        when caches are given, zero those pages.  Returns the new tags each
+        new owner records (0 for ids outside the pool)."""
+        assert page_tags.dtype == np.uint32 and page_tags.flags.c_contiguous
+        pg = _c(pages, np.int32)
+        new = np.zeros(pg.size, np.uint32)
+        if k_cache is not None:
+            P, Hkv, S, D = k_cache.shape
+            eb = k_cache.dtype.itemsize
+            assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        else:
+            Hkv, S, D, eb = 1, 1, 1, 1
+        self.lib.oracle_kv_page_realloc(_ptr(page_tags), int(page_tags.size), _ptr(pg), int(pg.size), _ptr(new),
+                                        _ptr(k_cache), _ptr(v_cache), Hkv, S, D, eb)
+        return new
 
     def dense_attn(self, q, k, v, sm_scale) -> np.ndarray:
         q, k, v = _c(q, np.float64), _c(k, np.float64), _c(v, np.float64)

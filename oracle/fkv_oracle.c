@@ -330,3 +330,30 @@ void oracle_paged_decode_attn(const uint16_t *q, int32_t batch, int32_t num_q_he
         free(vd);
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Reallocation: hand pages to new owners.  [GN], [CF]: a page's tag changes */
+/* each time the page is reallocated, so holders of the old (page, tag) pair */
+/* fail the check.  Optional scrub zeroes the page's K and V bytes first.    */
+/* ------------------------------------------------------------------------ */
+void oracle_kv_page_realloc(uint32_t *page_tags, int32_t num_pages,
+                            const int32_t *pages, int32_t n, uint32_t *new_tags,
+                            uint8_t *k_cache, uint8_t *v_cache,
+                            int32_t num_kv_heads, int32_t page_size, int32_t head_dim,
+                            int32_t elem_bytes)
+{
+    int64_t page_bytes = (int64_t)num_kv_heads * page_size * head_dim * elem_bytes;
+    for (int32_t j = 0; j < n; ++j) {
+        int32_t p = pages[j];
+        if (p < 0 || p >= num_pages) {
+            new_tags[j] = 0;               /* not a page of this pool: nothing changes */
+            continue;
+        }
+        page_tags[p] = page_tags[p] + 1u;  /* 32-bit wrap counts as a change */
+        new_tags[j] = page_tags[p];
+        if (k_cache && v_cache) {
+            memset(k_cache + (int64_t)p * page_bytes, 0, (size_t)page_bytes);
+            memset(v_cache + (int64_t)p * page_bytes, 0, (size_t)page_bytes);
+        }
+    }
+}

@@ -229,6 +229,55 @@ def pin_tag_check_page_range(orc):
     assert got.tolist() == [0, 1, 1]
 
 
+def pin_realloc_aborts_exactly_old_holders(orc):
+    """Reallocating pages (tag + 1, [GN]/[CF]) makes every request holding one
+    of them fail the check, and a request that records the new tags passes."""
+    rng = np.random.default_rng(31)
+    P, B = 50, 10
+    tags = rng.integers(0, 2 ** 32, P, dtype=np.uint64).astype(np.uint32)
+    tags[3] = 0xFFFFFFFF
+    counts = rng.integers(1, 8, B)
+    indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    indices = rng.integers(0, P, int(indptr[-1])).astype(np.int32)
+    indices[0] = 3
+    expected = tags[indices].copy()
+    moved = np.array([3, int(indices[5]), 17, P + 2, -1], np.int32)
+    live = tags.copy()
+    new = orc.kv_page_realloc(live, moved)
+    for j, p in enumerate(moved):
+        if 0 <= p < P:
+            bumps = 1 + int((moved[:j] == p).sum())
+            assert int(new[j]) == (int(tags[p]) + bumps) & 0xFFFFFFFF, "tag moves on by one per reallocation"
+        else:
+            assert new[j] == 0
+    assert live[3] == 0, "0xFFFFFFFF wraps to 0"
+    in_pool = moved[(moved >= 0) & (moved < P)]
+    untouched = np.setdiff1d(np.arange(P), in_pool)
+    assert np.array_equal(live[untouched], tags[untouched])
+    got = orc.kv_page_tag_check(live, indptr, indices, expected)
+    want = np.array([np.isin(indices[indptr[r]:indptr[r + 1]], in_pool).any() for r in range(B)], np.uint8)
+    assert np.array_equal(got, want)
+    # a new owner of page 17 that records the new tag passes
+    ok = orc.kv_page_tag_check(live, np.array([0, 1], np.int32), np.array([17], np.int32),
+                               np.array([new[2]], np.uint32))
+    assert ok.tolist() == [0]
+
+
+def pin_realloc_scrub_zeroes_listed_pages(orc):
+    rng = np.random.default_rng(32)
+    for dt in (np.uint8, np.uint16):
+        kc = rng.integers(1, 200, (6, 2, 16, 128)).astype(dt)
+        vc = rng.integers(1, 200, (6, 2, 16, 128)).astype(dt)
+        k0, v0 = kc.copy(), vc.copy()
+        tags = np.arange(6, dtype=np.uint32)
+        orc.kv_page_realloc(tags, np.array([4, 1, 9], np.int32), kc, vc)
+        for p in range(6):
+            if p in (1, 4):
+                assert not kc[p].any() and not vc[p].any()
+            else:
+                assert np.array_equal(kc[p], k0[p]) and np.array_equal(vc[p], v0[p])
+
+
 def pin_tag_check_malformed(orc):
     tags = np.array([1, 2], np.uint32)
     got = orc.kv_page_tag_check(tags, np.array([0, 2, 1], np.int32), np.array([0, 1], np.int32),

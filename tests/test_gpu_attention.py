@@ -18,6 +18,7 @@ SHAPES = [
     (3, 4, 2, 128, [300, 129, 5]),           # G = 2
     (2, 16, 2, 64, [40000, 12345]),          # long: split over many warps
     (5, 32, 8, 16, [4097, 1, 2, 3000, 16]),
+    (3, 6, 2, 32, [700, 64, 129]),           # G = 3 (N padded to 8)
 ]
 
 
@@ -133,3 +134,45 @@ def test_empty_batch_is_noop():
     fkv.paged_decode_attn(q, kc, kc, i1, i1, i1[:0], 0.1, q, ws, k_scale=s, v_scale=s)
     torch.cuda.synchronize()
 
+
+
+def test_graph_captured_step_equals_eager(orc):
+    """The step captured in a CUDA graph (append, check, attention) gives the
+    same bytes as the eager calls."""
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    from fp8_paged_kv_decode_gb300 import workloads as W
+    wl = W.WORKLOADS["integrity_256req"]
+    db = W.device_batch(wl, "cuda", ctx=np.full(wl.batch, 300))
+    P = db.pt.num_pages
+    kc = torch.zeros(P, wl.num_kv_heads, wl.page_size, 128, dtype=torch.uint8, device="cuda")
+    vc = torch.zeros_like(kc)
+    ks, vs = dev(db.k_scale), dev(db.v_scale)
+    fkv.kv_append_fp8(db.k_src, db.v_src, db.slots_src, ks, vs, kc, vc)
+    ind, indp = dev(db.pt.indices), dev(db.pt.indptr)
+    tags, exp = dev(db.pt.page_tags.view(np.int32)), dev(db.pt.expected_tags.view(np.int32))
+    seq = dev(db.seq_lens)
+    mask = torch.zeros(wl.batch, dtype=torch.uint8, device="cuda")
+    out = torch.zeros(wl.batch, wl.num_q_heads, 128, dtype=torch.bfloat16, device="cuda")
+    ws = fkv.alloc_workspace(wl.batch, wl.num_q_heads, wl.num_kv_heads)
+
+    def step():
+        fkv.kv_append_fp8(db.k_new, db.v_new, db.slots_new, ks, vs, kc, vc)
+        fkv.kv_page_tag_check(tags, indp, ind, exp, mask)
+        fkv.paged_decode_attn(db.q, kc, vc, indp, ind, seq, 1 / np.sqrt(128), out, ws, k_scale=ks, v_scale=vs,
+                              abort_mask=mask)
+
+    step()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    out.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(mask.sum()) > 0
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))

@@ -39,6 +39,8 @@ MUTANTS = {
                                 "kd[(int64_t)t * D + d] = cache_value(k_cache, kv_is_fp8, base + d, v_scale, h);"),
     "attn_ignores_abort": ("if (abort_mask && abort_mask[r])", "if (0)"),
     "attn_ignores_nnz": ("page_indptr[r + 1] > nnz)", "page_indptr[r + 1] > nnz + 1000000)"),
+    "realloc_no_bump": ("page_tags[p] = page_tags[p] + 1u;", "page_tags[p] = page_tags[p] + 0u;"),
+    "realloc_scrub_wrong_page": ("memset(k_cache + (int64_t)p * page_bytes", "memset(k_cache + (int64_t)(p + 1) * page_bytes"),
     "attn_last_token_dropped": ("for (int32_t t = 0; t < T; ++t) {\n            int64_t page",
                                 "for (int32_t t = 0; t < T - 1; ++t) {\n            int64_t page"),
 }
