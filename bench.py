@@ -287,6 +287,33 @@ class Step:
         barrier()
         return t0.elapsed_time(t1)
 
+    def time_prefill(self, reps=3):
+        """Bulk write of the whole cached context as a prefill would hand it
+        over: kv_calibrate_scales on the bf16 prompt, then kv_append_fp8 of
+        every token (rewrites the same bytes)."""
+        torch, fkv = self.torch, self.fkv
+        db = self.db
+        ks = torch.empty_like(self.k_scale)
+        vs = torch.empty_like(self.v_scale)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        cal, app = [], []
+        for _ in range(reps + 1):
+            ev[0].record()
+            fkv.kv_calibrate_scales(db.k_src, db.v_src, ks, vs)
+            ev[1].record()
+            fkv.kv_append_fp8(db.k_src, db.v_src, db.slots_src, ks, vs, self.k_cache, self.v_cache)
+            ev[2].record()
+            torch.cuda.synchronize(self.device)
+            cal.append(ev[0].elapsed_time(ev[1]))
+            app.append(ev[1].elapsed_time(ev[2]))
+        cal_ms, app_ms = float(np.median(cal[1:])), float(np.median(app[1:]))
+        ntok = int(db.slots_src.numel())
+        src = 2 * ntok * self.Hkv * self.D * 2
+        same = bool(torch.equal(ks, self.k_scale) and torch.equal(vs, self.v_scale))
+        return {"tokens": ntok, "calibrate_ms": cal_ms, "calibrate_gbs": src / (cal_ms * 1e6),
+                "bulk_append_ms": app_ms, "bulk_append_gbs": (src + src // 2) / (app_ms * 1e6),
+                "scales_equal_harness": same}
+
     def time_realloc(self, frac, reps):
         """kv_page_realloc of a seeded ``frac`` of the in-use pages, with and
         without the scrub of their K and V bytes (CUDA-graph timed)."""
@@ -555,6 +582,7 @@ def main():
     }
 
     if not args.skip_extras and args.kv == "fp8":
+        line["prefill_bulk_write"] = fp8.time_prefill()
         bf = Step(db, "bf16", device)
         bms, battn = bf.timed(max(10, args.steps // 2), args.warmup)
         bms, battn = max_over_ranks(bms), max_over_ranks(battn)

@@ -8,6 +8,7 @@ the library is missing or no GPU is present the calls raise.
 
 Entry points (same names as the C ABI):
   kv_append_fp8 / kv_append_bf16   write new tokens into the paged pools
+  kv_calibrate_scales              per-KV-head FP8 scales of a prompt (bulk write)
   kv_page_tag_check                the separate per-page generation-tag check
   kv_page_realloc                  bump tags (and optionally zero pages) of reallocated pages
   paged_decode_attn                decode attention over the paged cache
@@ -21,7 +22,8 @@ import threading
 
 __all__ = [
     "FkvError", "KV_FP8_E4M3", "KV_BF16", "library_path", "load_library", "kv_append_fp8", "kv_append_bf16",
-    "kv_page_tag_check", "kv_page_realloc", "paged_decode_attn", "paged_decode_attn_workspace_size",
+    "kv_calibrate_scales", "kv_page_tag_check", "kv_page_realloc", "paged_decode_attn",
+    "paged_decode_attn_workspace_size",
     "alloc_workspace",
     "paged_decode_attn_noalloc",
     "device_error", "kernels_per_call", "EXPORTED_SYMBOLS",
@@ -36,7 +38,8 @@ DEVERR_REALLOC_PAGE = 0x8
 HEAD_DIM = 128
 
 EXPORTED_SYMBOLS = (
-    "fkv_status_string", "kv_append_fp8", "kv_append_bf16", "kv_page_tag_check", "kv_page_realloc",
+    "fkv_status_string", "kv_append_fp8", "kv_append_bf16", "kv_calibrate_scales", "kv_page_tag_check",
+    "kv_page_realloc",
     "paged_decode_attn_workspace_size", "paged_decode_attn", "paged_decode_attn_noalloc", "fkv_device_error",
     "fkv_kernels_per_call",
 )
@@ -75,6 +78,8 @@ def load_library():
         lib.kv_append_bf16.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, P]
         lib.kv_page_tag_check.restype = ctypes.c_int
         lib.kv_page_tag_check.argtypes = [P, i32, P, P, P, i32, i64, P, P]
+        lib.kv_calibrate_scales.restype = ctypes.c_int
+        lib.kv_calibrate_scales.argtypes = [P, P, i64, i32, i32, P, P, P]
         lib.kv_page_realloc.restype = ctypes.c_int
         lib.kv_page_realloc.argtypes = [P, i32, P, i32, P, P, P, i32, i32, i32, i32, P]
         lib.paged_decode_attn_workspace_size.restype = ctypes.c_size_t
@@ -176,6 +181,19 @@ def kv_page_tag_check(page_tags, page_indptr, page_indices, expected_tags, abort
     _raise(load_library().kv_page_tag_check(_ptr(page_tags), page_tags.numel(), _ptr(page_indptr),
                                             _ptr(page_indices), _ptr(expected_tags), B, page_indices.numel(),
                                             _ptr(abort_mask), _stream(stream)), "kv_page_tag_check")
+
+
+def kv_calibrate_scales(k, v, k_scale, v_scale, stream=None):
+    """Per-KV-head scales fl32(amax / 448) of a prompt's bf16 K/V [N][Hkv][128]
+    (1 for an all-zero head), written into ``k_scale``/``v_scale`` (fp32 [Hkv])."""
+    import torch
+    _dev(k, v, k_scale, v_scale)
+    _need(k.dtype == torch.bfloat16 and v.dtype == torch.bfloat16, "k/v must be bf16")
+    _need(k_scale.dtype == torch.float32 and v_scale.dtype == torch.float32, "scales must be float32")
+    N, Hkv, D = k.shape
+    _need(tuple(v.shape) == (N, Hkv, D) and k_scale.numel() == Hkv and v_scale.numel() == Hkv, "shape mismatch")
+    _raise(load_library().kv_calibrate_scales(_ptr(k), _ptr(v), N, Hkv, D, _ptr(k_scale), _ptr(v_scale),
+                                              _stream(stream)), "kv_calibrate_scales")
 
 
 def kv_page_realloc(page_tags, pages, new_tags, k_cache=None, v_cache=None, stream=None):

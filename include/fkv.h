@@ -114,6 +114,25 @@ FKV_API fkv_status kv_append_bf16(const void *k_new, const void *v_new,
                           int32_t page_size, int32_t head_dim, void *stream);
 
 /*
+ * kv_calibrate_scales -- the per-KV-head scales for writing a whole prompt
+ * into the FP8 cache (Cloudflare post: prefill keeps BF16, the cache decode
+ * reads is FP8 e4m3).  For each KV head h, separately for K and for V:
+ *     amax = max |x| over all n_tokens tokens and head_dim elements of head h
+ *     scale[h] = fl32(amax / 448)  (IEEE division; 448 = largest e4m3 value),
+ *                1 when amax is 0 (including n_tokens == 0)
+ * then kv_append_fp8 with these scales quantizes the prompt (bulk write).
+ *
+ *   k, v      bf16 [n_tokens][num_kv_heads][head_dim], finite values
+ *             (a NaN or Inf input gives a NaN or Inf scale)
+ *   k_scale, v_scale  fp32 [num_kv_heads] outputs (also used as the
+ *             reduction's scratch; nothing else is written)
+ * Launches two kernels and two memsets on `stream`.
+ */
+FKV_API fkv_status kv_calibrate_scales(const void *k, const void *v, int64_t n_tokens,
+                                       int32_t num_kv_heads, int32_t head_dim,
+                                       float *k_scale, float *v_scale, void *stream);
+
+/*
  * kv_page_tag_check -- the separate batched integrity pass ("Kimi and GLM
  * Reasoning Slimming: Hands-On Test", section "Giving Every Physical Cache
  * Page a 'Generation Number'"; Cloudflare post, integrity checking).  For each

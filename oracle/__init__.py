@@ -16,6 +16,8 @@ Parity status of each function (what pins it independently of itself is in
   against a hand-computed position, untouched bytes.
 * ``kv_page_tag_check`` -- pinned: hand-derived cases in ``tests/golden``,
   brute force, tag bump and 32-bit wrap-around.
+* ``kv_calibrate_scales`` -- pinned: numpy's max of |x| and IEEE float32
+  division; all-zero heads; a single outlier sets its head's scale.
 * ``kv_page_realloc`` -- pinned: reallocation then the (pinned) tag check
   aborts exactly the old holders; a fresh holder of the new tag passes;
   wrap-around; scrub zeroes exactly the listed pages.
@@ -92,6 +94,8 @@ class Oracle:
         lib.oracle_paged_decode_attn.argtypes = [
             P, i32, i32, P, P, i32, P, P, i32, i32, i32, i32,
             P, P, i64, P, P, ctypes.c_double, P, i32, P]
+        lib.oracle_kv_calibrate_scales.restype = None
+        lib.oracle_kv_calibrate_scales.argtypes = [P, P, i64, i32, i32, P, P]
         lib.oracle_kv_page_realloc.restype = None
         lib.oracle_kv_page_realloc.argtypes = [P, i32, P, i32, P, P, P, i32, i32, i32, i32]
         self.lib = lib
@@ -154,6 +158,16 @@ class Oracle:
         self.lib.oracle_kv_page_tag_check(_ptr(tags), P, _ptr(indptr), _ptr(indices),
                                           _ptr(exp), B, int(indices.size), _ptr(out))
         return out
+
+    def kv_calibrate_scales(self, k, v):
+        """Per-KV-head scales fl32(amax / 448) (1 for an all-zero head) of bf16
+        ``k``/``v`` [N][Hkv][D] (uint16 bits)."""
+        kk, vv = _c(k, np.uint16), _c(v, np.uint16)
+        N, Hkv, D = kk.shape
+        ks = np.zeros(Hkv, np.float32)
+        vs = np.zeros(Hkv, np.float32)
+        self.lib.oracle_kv_calibrate_scales(_ptr(kk), _ptr(vv), N, Hkv, D, _ptr(ks), _ptr(vs))
+        return ks, vs
 
     def kv_page_realloc(self, page_tags, pages, k_cache=None, v_cache=None):
         """In place: bump the live tag of every listed page (uint32, wraps) and,

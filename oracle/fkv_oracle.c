@@ -357,3 +357,28 @@ void oracle_kv_page_realloc(uint32_t *page_tags, int32_t num_pages,
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Scale calibration for a bulk (prefill) write: per KV head, the largest    */
+/* |value| over all tokens, scale = fl32(amax / 448) (448 = the largest      */
+/* finite e4m3 magnitude), 1 when the head is all zeros.                     */
+/* ------------------------------------------------------------------------ */
+void oracle_kv_calibrate_scales(const uint16_t *k, const uint16_t *v, int64_t n_tokens,
+                                int32_t num_kv_heads, int32_t head_dim,
+                                float *k_scale, float *v_scale)
+{
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+        double ka = 0.0, va = 0.0;
+        for (int64_t n = 0; n < n_tokens; ++n) {
+            for (int32_t d = 0; d < head_dim; ++d) {
+                int64_t i = (n * num_kv_heads + h) * head_dim + d;
+                double a = fabs(oracle_bf16_to_double(k[i]));
+                double b = fabs(oracle_bf16_to_double(v[i]));
+                if (a > ka) ka = a;
+                if (b > va) va = b;
+            }
+        }
+        k_scale[h] = ka > 0.0 ? (float)(ka / 448.0) : 1.0f;
+        v_scale[h] = va > 0.0 ? (float)(va / 448.0) : 1.0f;
+    }
+}

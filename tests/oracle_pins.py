@@ -278,6 +278,32 @@ def pin_realloc_scrub_zeroes_listed_pages(orc):
                 assert np.array_equal(kc[p], k0[p]) and np.array_equal(vc[p], v0[p])
 
 
+def pin_calibration_scales(orc):
+    """fl32(amax / 448) per KV head against numpy; zero heads give 1; one
+    outlier decides its head; and the resulting codes reach 448 exactly."""
+    rng = np.random.default_rng(33)
+    N, Hkv, D = 257, 4, 128
+    kf = rng.standard_normal((N, Hkv, D)).astype(np.float32)
+    vf = (rng.standard_normal((N, Hkv, D)) * 0.01).astype(np.float32)
+    kf[:, 2, :] = 0.0                       # all-zero heads
+    vf[:, 3, :] = 0.0
+    kf[100, 1, 7] = -3.0e4                  # one outlier
+    kb, vb = bf16_bits(kf), bf16_bits(vf)
+    ks, vs = orc.kv_calibrate_scales(kb, vb)
+    for bits, got in ((kb, ks), (vb, vs)):
+        amax = np.abs(bits_to_f32(bits)).max(axis=(0, 2))
+        want = np.where(amax > 0, (amax / np.float32(448.0)).astype(np.float32), np.float32(1.0))
+        assert np.array_equal(got.view(np.uint32), want.astype(np.float32).view(np.uint32))
+    assert ks[2] == 1.0 and vs[3] == 1.0
+    assert ks[1] == np.float32(np.float32(bits_to_f32(kb[100, 1, 7:8])[0] * -1) / np.float32(448.0))
+    # quantizing with the calibrated scale maps each head's largest value to the largest code
+    P = 1
+    kc = np.zeros((P, Hkv, 16, D), np.uint8)
+    vc = np.zeros((P, Hkv, 16, D), np.uint8)
+    orc.kv_append_fp8(kb[100:101], vb[100:101], np.array([0]), ks, vs, kc, vc)
+    assert kc[0, 1, 0, 7] == 0xFE           # -448
+
+
 def pin_tag_check_malformed(orc):
     tags = np.array([1, 2], np.uint32)
     got = orc.kv_page_tag_check(tags, np.array([0, 2, 1], np.int32), np.array([0, 1], np.int32),

@@ -41,6 +41,8 @@ MUTANTS = {
     "attn_ignores_nnz": ("page_indptr[r + 1] > nnz)", "page_indptr[r + 1] > nnz + 1000000)"),
     "realloc_no_bump": ("page_tags[p] = page_tags[p] + 1u;", "page_tags[p] = page_tags[p] + 0u;"),
     "realloc_scrub_wrong_page": ("memset(k_cache + (int64_t)p * page_bytes", "memset(k_cache + (int64_t)(p + 1) * page_bytes"),
+    "calib_wrong_max_code": ("k_scale[h] = ka > 0.0 ? (float)(ka / 448.0) : 1.0f;", "k_scale[h] = ka > 0.0 ? (float)(ka / 240.0) : 1.0f;"),
+    "calib_zero_head_scale": ("v_scale[h] = va > 0.0 ? (float)(va / 448.0) : 1.0f;", "v_scale[h] = va > 0.0 ? (float)(va / 448.0) : 0.0f;"),
     "attn_last_token_dropped": ("for (int32_t t = 0; t < T; ++t) {\n            int64_t page",
                                 "for (int32_t t = 0; t < T - 1; ++t) {\n            int64_t page"),
 }
