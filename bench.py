@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--kv", default="fp8", choices=["fp8", "bf16"], help="KV cache dtype of the main line")
     ap.add_argument("--skip-extras", action="store_true", help="only the FP8 headline and e2e")
     ap.add_argument("--cpu-requests", type=int, default=4, help="requests in the oracle's bounded sample")
+    ap.add_argument("--capacity-sweep", action="store_true",
+                    help="instead of the headline: KV budget admission and a concurrency sweep, FP8 vs BF16")
     return ap.parse_args()
 
 
@@ -255,12 +257,17 @@ class Step:
         attn_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
         return total_ms, attn_ms
 
-    def graph(self, with_check=True, checks_only=0):
-        """One step (or ``checks_only`` back-to-back checks) captured in a CUDA
-        graph, so host launch cost is out of the measurement."""
+    def graph(self, with_check=True, checks_only=0, attn_only=False):
+        """One step (or ``checks_only`` back-to-back checks, or the attention
+        call alone) captured in a CUDA graph, so host launch cost is out of
+        the measurement."""
         torch = self.torch
-        body = (lambda: [self.check() for _ in range(checks_only)]) if checks_only else \
-            (lambda: (self.append(), self.check() if with_check else None, self.attend(with_check)))
+        if attn_only:
+            body = lambda: self.attend(True)
+        elif checks_only:
+            body = lambda: [self.check() for _ in range(checks_only)]
+        else:
+            body = lambda: (self.append(), self.check() if with_check else None, self.attend(with_check))
         body()                                    # one-time set-up happens outside the capture
         torch.cuda.synchronize(self.device)
         s = torch.cuda.Stream(self.device)
@@ -271,9 +278,9 @@ class Step:
         torch.cuda.synchronize(self.device)
         return g
 
-    def timed_graph(self, steps, warmup, with_check=True, checks_only=0):
+    def timed_graph(self, steps, warmup, with_check=True, checks_only=0, attn_only=False):
         torch = self.torch
-        g = self.graph(with_check, checks_only)
+        g = self.graph(with_check, checks_only, attn_only)
         for _ in range(warmup):
             g.replay()
         torch.cuda.synchronize(self.device)
@@ -516,11 +523,58 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def capacity_sweep(args):
+    """A per-layer KV budget that holds the first 32 requests of the 64-request
+    workload in BF16; how many requests each KV dtype admits under it, and the
+    decode step (append + check + attention) at concurrency 1..64 for both,
+    for the concurrencies each dtype can hold.  Steps are CUDA-graph captured
+    so small batches measure GPU time, not host launch cost."""
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    from fp8_paged_kv_decode_gb300 import workloads as W
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    fkv.load_library()
+    wl = W.WORKLOADS[HEADLINE]
+    db = W.device_batch(wl, device)
+    npages = np.diff(db.pt.indptr)
+    page_fp8 = 2 * wl.num_kv_heads * wl.page_size * wl.head_dim
+    page_bf16 = 2 * page_fp8
+    budget = int(npages[:32].sum()) * page_bf16
+    adm = {"fp8": W.admitted(page_fp8, npages, budget), "bf16": W.admitted(page_bf16, npages, budget)}
+    rows = []
+    steps = max(50, args.steps // 10)
+    for c in sorted({1, 2, 4, 8, 16, 32, 48, 64, adm["fp8"], adm["bf16"]} - {0}):
+        row = {"requests": c, "tokens": int(db.seq_lens[:c].sum())}
+        sub = W.subset_batch(db, c)
+        for kv in ("fp8", "bf16"):
+            if c > adm[kv]:
+                row[kv] = None                      # does not fit the budget
+                continue
+            st = Step(sub, kv, device)
+            tot = st.timed_graph(steps, args.warmup)                 # whole step, CUDA graph
+            attn = st.timed_graph(steps, args.warmup, attn_only=True)
+            row[kv] = {"step_ms": tot / steps, "tokens_per_s": c / (tot / steps / 1e3), "attn_ms": attn / steps}
+            del st
+            torch.cuda.empty_cache()
+        rows.append(row)
+    peak = {kv: max((r[kv]["tokens_per_s"] for r in rows if r[kv]), default=0.0) for kv in ("fp8", "bf16")}
+    print(json.dumps({"capacity_sweep": {
+        "workload": workload_text(wl, db), "budget_bytes_per_layer": budget,
+        "budget": "BF16 pages of the first 32 requests", "admitted": adm,
+        "resident_tokens": {kv: int(db.seq_lens[:adm[kv]].sum()) for kv in adm},
+        "rows": rows, "peak_tokens_per_s": peak, "fp8_peak_over_bf16_peak": peak["fp8"] / peak["bf16"]}}),
+        flush=True)
+
+
 def main():
     global _PG
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.capacity_sweep:
+        capacity_sweep(args)
         return
     world, rank, local = dist_env()
     import torch

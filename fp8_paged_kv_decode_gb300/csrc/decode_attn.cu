@@ -62,6 +62,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;     // a copy that has not land
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kChunk = 6;                // parts merged per first-level merge of a long unit
+constexpr int kMinTilesPerWarp = 8;      // small batches use fewer, longer warp ranges
 
 template <bool kFp8>
 struct Cfg;
@@ -99,7 +100,7 @@ struct AttnParams {
     const int32_t *indices;
     const int32_t *seq_lens;
     const int64_t *prefix;     // [B+1] tile prefix over requests (tiles x Hkv)
-    const int32_t *warp_req;   // [NW] request holding each warp's first tile
+    const int32_t *warp_req;   // [NW + 1] request holding each warp's first tile; [NW] = warps with work
     float *part_o;             // [slots][G][D]   slots = B*Hkv + NW
     float2 *part_ml;           // [slots][G]  (m in log2 units, l; l < 0 marks an invalid unit)
     int32_t *counters;         // [B*Hkv] arrivals per split unit (or per chunk of it)
@@ -168,8 +169,14 @@ attn_plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict
     __syncthreads();
     const int64_t T = carry;
     const bool in_smem = B <= kPlanSmemPrefix;
-    for (int w = tid; w < NW; w += kPlanThreads) {
-        const int64_t lo = static_cast<int64_t>(w) * T / NW;
+    // Warps that get work: every one streams at least kMinTilesPerWarp tiles,
+    // so a small batch is not split into ranges too short to pay for their
+    // start-up and merge (large batches use all NW).
+    int64_t nw64 = (T + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
+    const int nw = static_cast<int>(nw64 < 1 ? 1 : (nw64 > NW ? NW : nw64));
+    if (tid == 0) warp_req[NW] = nw;
+    for (int w = tid; w < nw; w += kPlanThreads) {
+        const int64_t lo = static_cast<int64_t>(w) * T / nw;
         int res = B;
         if (lo < T) {
             int a = 0, z = B;                              // invariant: prefix[a] <= lo < prefix[z]
@@ -231,70 +238,106 @@ __device__ __forceinline__ int64_t warp_of_tile(int64_t x, int64_t T, int NW) {
 // `maybe_empty` (tiles < warps) entries of warps with an empty range, which
 // wrote nothing, are skipped; entry j belongs to warp wk0 + j.
 //
-// Lanes cover (entry, head) pairs for the softmax statistics (lane = k*8 + hd,
-// four entries per pass), so every head's max and sum come from one round of
-// loads and shuffles; the output pass keeps the loads of all heads of an entry
-// in flight together (lane = 4 output dims).
-__device__ void merge_parts(const AttnParams &p, int64_t slot0, int n, int stride, bool maybe_empty, int64_t wk0,
-                            int64_t T, bool final_out, int r, int h, float vsc, int64_t dst) {
+// Latency matters more than bandwidth here (a few KB per entry), so the
+// statistics of up to 32 entries come in one round of loads (lane = entry,
+// all heads per lane) and the output pass keeps two entries' loads (all heads,
+// 4 dims per lane) in flight.
+__device__ void merge_parts(const AttnParams &p, int nw, int64_t slot0, int n, int stride, bool maybe_empty,
+                            int64_t wk0, int64_t T, bool final_out, int r, int h, float vsc, int64_t dst) {
     const int lane = threadIdx.x;
     const int G = p.G;
     auto empty = [&](int j) {
-        return maybe_empty && warp_lo(wk0 + j, T, p.NW) == warp_lo(wk0 + j + 1, T, p.NW);
+        return maybe_empty && warp_lo(wk0 + j, T, nw) == warp_lo(wk0 + j + 1, T, nw);
     };
-    const int hd_l = lane & 7, k_l = lane >> 3;
-    // pass 1: per-head max and invalid flag
-    float mmax = -INFINITY;
+    auto slot_of = [&](int j) { return slot0 + static_cast<int64_t>(j) * stride; };
+    // statistics: per-head max, invalid flag, then normaliser
+    float M[kMaxGroup], L[kMaxGroup];
+#pragma unroll
+    for (int hd = 0; hd < kMaxGroup; ++hd) {
+        M[hd] = -INFINITY;
+        L[hd] = 0.f;
+    }
     bool bad = false;
-    for (int k0 = 0; k0 < n; k0 += 4) {
-        const int k = k0 + k_l;
-        if (hd_l < G && k < n && !empty(k)) {
-            const float2 ml = __ldcg(p.part_ml + (slot0 + static_cast<int64_t>(k) * stride) * G + hd_l);
-            bad |= ml.y < 0.f;
-            mmax = fmaxf(mmax, ml.x);
+    for (int k0 = 0; k0 < n; k0 += 32) {
+        const int k = k0 + lane;
+        if (k < n && !empty(k)) {
+#pragma unroll
+            for (int hd = 0; hd < kMaxGroup; ++hd) {
+                if (hd >= G) break;
+                const float2 ml = __ldcg(p.part_ml + slot_of(k) * G + hd);
+                bad |= ml.y < 0.f;
+                M[hd] = fmaxf(M[hd], ml.x);
+            }
         }
     }
-    mmax = fmaxf(mmax, __shfl_xor_sync(kFull, mmax, 8));
-    mmax = fmaxf(mmax, __shfl_xor_sync(kFull, mmax, 16));
+#pragma unroll
+    for (int hd = 0; hd < kMaxGroup; ++hd)
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) M[hd] = fmaxf(M[hd], __shfl_xor_sync(kFull, M[hd], o));
     bad = __any_sync(kFull, bad);
-    // pass 2: per-head normaliser
-    float ltot = 0.f;
-    for (int k0 = 0; k0 < n; k0 += 4) {
-        const int k = k0 + k_l;
-        if (hd_l < G && k < n && !empty(k)) {
-            const float2 ml = __ldcg(p.part_ml + (slot0 + static_cast<int64_t>(k) * stride) * G + hd_l);
-            ltot += ex2(ml.x - mmax) * ml.y;
+    float F[kMaxGroup];                                  // this lane's entry weights (first 32 entries)
+#pragma unroll
+    for (int hd = 0; hd < kMaxGroup; ++hd) F[hd] = 0.f;
+    for (int k0 = 0; k0 < n; k0 += 32) {
+        const int k = k0 + lane;
+        if (k < n && !empty(k)) {
+#pragma unroll
+            for (int hd = 0; hd < kMaxGroup; ++hd) {
+                if (hd >= G) break;
+                const float2 ml = __ldcg(p.part_ml + slot_of(k) * G + hd);
+                const float f = ex2(ml.x - M[hd]);
+                L[hd] += f * ml.y;
+                if (k0 == 0) F[hd] = f;
+            }
         }
     }
-    ltot += __shfl_xor_sync(kFull, ltot, 8);
-    ltot += __shfl_xor_sync(kFull, ltot, 16);
-    // pass 3: weighted sum of the partial outputs, 4 dims per lane, all heads at once
+#pragma unroll
+    for (int hd = 0; hd < kMaxGroup; ++hd)
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) L[hd] += __shfl_xor_sync(kFull, L[hd], o);
+    // weighted sum of the entries' outputs, 4 dims per lane, two entries in flight
     float4 acc[kMaxGroup];
 #pragma unroll
     for (int hd = 0; hd < kMaxGroup; ++hd) acc[hd] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (!bad) {
-        for (int k = 0; k < n; ++k) {
-            if (empty(k)) continue;
-            const int64_t slot = slot0 + static_cast<int64_t>(k) * stride;
-            float2 mlv = make_float2(-INFINITY, 0.f);
-            if (lane < G) mlv = __ldcg(p.part_ml + slot * G + lane);
+        for (int k = 0; k < n; k += 2) {
+            float fw[2][kMaxGroup];
+            float4 v[2][kMaxGroup];
 #pragma unroll
-            for (int hd = 0; hd < kMaxGroup; ++hd) {
-                if (hd >= G) break;
-                const float f = ex2(__shfl_sync(kFull, mlv.x, hd) - __shfl_sync(kFull, mmax, hd));
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (slot * G + hd) * kD) + lane);
-                acc[hd].x += f * v.x;
-                acc[hd].y += f * v.y;
-                acc[hd].z += f * v.z;
-                acc[hd].w += f * v.w;
+            for (int e = 0; e < 2; ++e) {
+                const int j = k + e;
+                const bool live = j < n && !empty(j);
+#pragma unroll
+                for (int hd = 0; hd < kMaxGroup; ++hd) {
+                    float f = 0.f;
+                    if (j < 32) {
+                        f = __shfl_sync(kFull, F[hd], j & 31);
+                    } else if (live && hd < G) {         // entries past the first 32: reload
+                        const float2 ml = __ldcg(p.part_ml + slot_of(j) * G + hd);
+                        f = ex2(ml.x - M[hd]);
+                    }
+                    fw[e][hd] = (live && hd < G) ? f : 0.f;
+                    v[e][hd] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (fw[e][hd] > 0.f)
+                        v[e][hd] = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (slot_of(j) * G + hd) * kD) + lane);
+                }
             }
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int hd = 0; hd < kMaxGroup; ++hd) {
+                    acc[hd].x += fw[e][hd] * v[e][hd].x;
+                    acc[hd].y += fw[e][hd] * v[e][hd].y;
+                    acc[hd].z += fw[e][hd] * v[e][hd].z;
+                    acc[hd].w += fw[e][hd] * v[e][hd].w;
+                }
         }
     }
     if (final_out) {
 #pragma unroll
         for (int hd = 0; hd < kMaxGroup; ++hd) {
             if (hd >= G) break;
-            const float sc = bad ? 0.f : vsc / __shfl_sync(kFull, ltot, hd);
+            const float sc = bad ? 0.f : vsc / L[hd];
             uint2 *orow =
                 reinterpret_cast<uint2 *>(p.out + (static_cast<int64_t>(r) * p.Hq + h * G + hd) * kD) + lane;
             *orow = make_uint2(pack_bf16x2(acc[hd].x * sc, acc[hd].y * sc),
@@ -306,7 +349,9 @@ __device__ void merge_parts(const AttnParams &p, int64_t slot0, int n, int strid
             if (hd >= G) break;
             __stcg(reinterpret_cast<float4 *>(p.part_o + (dst * G + hd) * kD) + lane, acc[hd]);
         }
-        if (lane < G) __stcg(p.part_ml + dst * G + lane, make_float2(mmax, bad ? -1.f : ltot));
+#pragma unroll
+        for (int hd = 0; hd < kMaxGroup; ++hd)
+            if (hd < G && lane == hd) __stcg(p.part_ml + dst * G + hd, make_float2(M[hd], bad ? -1.f : L[hd]));
     }
 }
 
@@ -338,14 +383,15 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     grid_dep_wait();                                   // plan results are visible
 
     const int64_t T = p.prefix[p.B];
+    const int nw = p.warp_req[p.NW];                   // warps with work (<= NW)
     // rows of requests with no tiles (aborted, empty, malformed) are zero
     for (int r = w; r < p.B; r += p.NW) {
         if (p.prefix[r + 1] != p.prefix[r]) continue;
         uint4 *orow = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(r) * p.Hq * kD);
         for (int c = lane; c < p.Hq * kD / 8; c += 32) orow[c] = make_uint4(0u, 0u, 0u, 0u);
     }
-    const int64_t lo = warp_lo(w, T, p.NW);
-    const int64_t hi = warp_lo(w + 1, T, p.NW);
+    const int64_t lo = w < nw ? warp_lo(w, T, nw) : 0;
+    const int64_t hi = w < nw ? warp_lo(w + 1, T, nw) : 0;
     if (lo >= hi) {
         grid_dep_launch();
         return;
@@ -752,22 +798,22 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                 // levels (chunks of kChunk consecutive parts, then the chunks),
                 // so no single warp reads a long unit's partials serially.
                 const int64_t s0 = p.prefix[C.r] + static_cast<int64_t>(C.h) * C.nt;
-                const int64_t wf = warp_of_tile(s0, T, p.NW), wl = warp_of_tile(s0 + C.nt - 1, T, p.NW);
+                const int64_t wf = warp_of_tile(s0, T, nw), wl = warp_of_tile(s0 + C.nt - 1, T, nw);
                 const int span = static_cast<int>(wl - wf + 1);
-                const bool maybe_empty = T < p.NW;
+                const bool maybe_empty = T < nw;
                 __threadfence();
                 __syncwarp();
                 if (maybe_empty || span <= kChunk) {
                     int nparts = span;
                     if (maybe_empty) {
                         nparts = 0;
-                        for (int64_t x = wf; x <= wl; ++x) nparts += warp_lo(x, T, p.NW) != warp_lo(x + 1, T, p.NW);
+                        for (int64_t x = wf; x <= wl; ++x) nparts += warp_lo(x, T, nw) != warp_lo(x + 1, T, nw);
                     }
                     int last = 0;
                     if (lane == 0) last = atomicAdd(p.counters + u, 1) == nparts - 1;
                     if (__shfl_sync(kFull, last, 0)) {
                         __threadfence();
-                        merge_parts(p, u + wf, span, 1, maybe_empty, wf, T, true, C.r, C.h, vsc, 0);
+                        merge_parts(p, nw, u + wf, span, 1, maybe_empty, wf, T, true, C.r, C.h, vsc, 0);
                     }
                 } else {
                     const int c0 = (static_cast<int>(w - wf) / kChunk) * kChunk;
@@ -777,14 +823,14 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                     if (lane == 0) last = atomicAdd(p.chunk_counters + (u + wf + c0), 1) == csz - 1;
                     if (__shfl_sync(kFull, last, 0)) {
                         __threadfence();
-                        merge_parts(p, u + wf + c0, csz, 1, false, wf + c0, T, false, C.r, C.h, vsc, u + wf + c0);
+                        merge_parts(p, nw, u + wf + c0, csz, 1, false, wf + c0, T, false, C.r, C.h, vsc, u + wf + c0);
                         __threadfence();
                         __syncwarp();
                         int last2 = 0;
                         if (lane == 0) last2 = atomicAdd(p.counters + u, 1) == nch - 1;
                         if (__shfl_sync(kFull, last2, 0)) {
                             __threadfence();
-                            merge_parts(p, u + wf, nch, kChunk, false, wf, T, true, C.r, C.h, vsc, 0);
+                            merge_parts(p, nw, u + wf, nch, kChunk, false, wf, T, true, C.r, C.h, vsc, 0);
                         }
                     }
                 }
@@ -857,7 +903,7 @@ WsLayout ws_layout(int B, int Hkv, int G, int NW) {
     const size_t slots = units + NW;
     L.prefix = 0;
     L.warp_req = align256(L.prefix + sizeof(int64_t) * (static_cast<size_t>(B) + 1));
-    L.counters = align256(L.warp_req + sizeof(int32_t) * NW);
+    L.counters = align256(L.warp_req + sizeof(int32_t) * (NW + 1));
     L.part_ml = align256(L.counters + sizeof(int32_t) * (units + slots));
     L.part_o = align256(L.part_ml + sizeof(float2) * slots * G);
     L.total = align256(L.part_o + sizeof(float) * slots * G * kD);

@@ -360,3 +360,29 @@ def compact_requests(db: DeviceBatch, reqs) -> CompactRequests:
         reqs=reqs, q=q, k_tokens=np.concatenate(ks), v_tokens=np.concatenate(vs), slots=np.concatenate(slots),
         indptr=np.array(indptr, np.int32), indices=np.arange(n_pages, dtype=np.int32),
         seq_lens=db.seq_lens[reqs].astype(np.int32), orig_pages=np.array(orig, np.int64), num_pages=n_pages)
+
+
+def subset_batch(db: DeviceBatch, n: int) -> DeviceBatch:
+    """The first ``n`` requests of a batch, same pool and page ids."""
+    import torch
+    pt = db.pt
+    nnz = int(pt.indptr[n])
+    ntok = int(db.ctx[:n].sum())
+    sub_pt = PageTable(pt.indptr[:n + 1].copy(), pt.indices[:nnz].copy(), pt.expected_tags[:nnz].copy(),
+                       pt.page_tags, pt.num_pages, pt.stale_pages)
+    wl = Workload(**{**db.wl.__dict__, "name": "%s[:%d]" % (db.wl.name, n), "batch": n})
+    return DeviceBatch(wl=wl, ctx=db.ctx[:n].copy(), seq_lens=db.seq_lens[:n].copy(), pt=sub_pt,
+                       tok_off=db.tok_off[:n].copy(), q=db.q[:n], k_src=db.k_src[:ntok], v_src=db.v_src[:ntok],
+                       slots_src=db.slots_src[:ntok], k_new=db.k_new[:n], v_new=db.v_new[:n],
+                       slots_new=db.slots_new[:n], k_scale=db.k_scale, v_scale=db.v_scale)
+
+
+def admitted(page_bytes: int, pages_per_request, budget_bytes: int) -> int:
+    """How many requests, taken in order, fit a KV budget (whole pages)."""
+    used, n = 0, 0
+    for p in pages_per_request:
+        if used + int(p) * page_bytes > budget_bytes:
+            break
+        used += int(p) * page_bytes
+        n += 1
+    return n

@@ -99,3 +99,19 @@ def test_replica_sharding_gloo_world2():
     for rank, cover, ms in res:
         assert cover == [1] * 64
         assert ms == 11.0
+
+
+def test_admission_under_a_budget():
+    pages = np.array([3, 1, 4, 1, 5])
+    assert W.admitted(10, pages, 0) == 0
+    assert W.admitted(10, pages, 40) == 2          # 3 + 1 pages fit, the third (4) does not
+    assert W.admitted(10, pages, 90) == 4
+    assert W.admitted(5, pages, 40) == 3           # half the page bytes: twice the pages
+    # the same budget holds twice the tokens at half the bytes per page
+    wl = W.WORKLOADS["pages_shaped_64req"]
+    rng = np.random.default_rng(wl.seed)
+    npg = (W.context_lengths(wl, rng) + 1 + 63) // 64
+    pf = 2 * 8 * 64 * 128
+    budget = int(npg[:32].sum()) * 2 * pf
+    assert W.admitted(2 * pf, npg, budget) == 32
+    assert W.admitted(pf, npg, budget) > 32
