@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--kv", default="fp8", choices=["fp8", "bf16"], help="KV cache dtype of the main line")
     ap.add_argument("--skip-extras", action="store_true", help="only the FP8 headline and e2e")
     ap.add_argument("--cpu-requests", type=int, default=4, help="requests in the oracle's bounded sample")
+    ap.add_argument("--shared-prefix", action="store_true",
+                    help="instead of the headline: requests sharing their first pages (a common prompt prefix)")
     ap.add_argument("--capacity-sweep", action="store_true",
                     help="instead of the headline: KV budget admission and a concurrency sweep, FP8 vs BF16")
     return ap.parse_args()
@@ -567,6 +569,41 @@ def capacity_sweep(args):
         flush=True)
 
 
+def shared_prefix(args):
+    """The 64-request workload with every request's first m pages replaced by
+    request 0's (a shared prompt prefix of m*64 tokens): decode step time,
+    bytes attended per second (each request's reads) and unique KV bytes
+    per second (what HBM must supply at least)."""
+    import dataclasses
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    from fp8_paged_kv_decode_gb300 import workloads as W
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    fkv.load_library()
+    wl = W.WORKLOADS[HEADLINE]
+    db = W.device_batch(wl, device)
+    n0 = int(db.pt.indptr[1] - db.pt.indptr[0])
+    steps = max(100, args.steps // 5)
+    rows = []
+    for m in sorted({0, 8, 32, 64, n0 - 1}):
+        sub = dataclasses.replace(db, pt=W.share_prefix(db.pt, m))
+        st = Step(sub, "fp8", device)
+        tot = st.timed_graph(steps, args.warmup)
+        attn = st.timed_graph(steps, args.warmup, attn_only=True) / steps
+        attended, _ = st.attn_bytes()
+        ind = sub.pt.indices
+        used = np.concatenate([ind[sub.pt.indptr[r]:sub.pt.indptr[r] + (int(sub.seq_lens[r]) + wl.page_size - 1)
+                                   // wl.page_size] for r in range(wl.batch)])
+        unique = np.unique(used).size * 2 * wl.num_kv_heads * wl.page_size * wl.head_dim
+        rows.append({"shared_prefix_tokens": m * wl.page_size, "step_ms": tot / steps, "attn_ms": attn,
+                     "attended_gbs": attended / (attn * 1e6), "unique_kv_bytes": int(unique),
+                     "unique_gbs": unique / (attn * 1e6)})
+        del st
+        torch.cuda.empty_cache()
+    print(json.dumps({"shared_prefix": {"workload": workload_text(wl, db), "rows": rows}}), flush=True)
+
+
 def main():
     global _PG
     args = parse()
@@ -575,6 +612,9 @@ def main():
         return
     if args.capacity_sweep:
         capacity_sweep(args)
+        return
+    if args.shared_prefix:
+        shared_prefix(args)
         return
     world, rank, local = dist_env()
     import torch

@@ -51,6 +51,10 @@
 #ifndef FKV_BF16_STAGES
 #define FKV_BF16_STAGES 2
 #endif
+// L2 hint of the K/V tile copies (streamed once unless pages are shared).
+#ifndef FKV_KV_EVICT_FIRST
+#define FKV_KV_EVICT_FIRST 1
+#endif
 
 namespace fkv {
 
@@ -397,7 +401,11 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
         return;
     }
     const int64_t n_tiles = hi - lo;
+#if FKV_KV_EVICT_FIRST
     const uint64_t policy = l2_policy_evict_first();
+#else
+    const uint64_t policy = l2_policy_evict_normal();
+#endif
 
     // ---------------- load side ----------------
     Cursor L;

@@ -386,3 +386,22 @@ def admitted(page_bytes: int, pages_per_request, budget_bytes: int) -> int:
         used += int(p) * page_bytes
         n += 1
     return n
+
+
+def share_prefix(pt: PageTable, prefix_pages: int) -> PageTable:
+    """Every request with more than ``prefix_pages`` pages reads request 0's
+    first ``prefix_pages`` pages (a shared prompt prefix) instead of its own;
+    its expected tags for them are request 0's.  Request 0 must hold at least
+    that many pages."""
+    indptr = pt.indptr
+    n0 = int(indptr[1] - indptr[0])
+    if prefix_pages > n0:
+        raise ValueError("request 0 holds fewer pages than the shared prefix")
+    ind, exp = pt.indices.copy(), pt.expected_tags.copy()
+    src = slice(int(indptr[0]), int(indptr[0]) + prefix_pages)
+    for r in range(1, indptr.size - 1):
+        a, b = int(indptr[r]), int(indptr[r + 1])
+        if b - a > prefix_pages:
+            ind[a:a + prefix_pages] = pt.indices[src]
+            exp[a:a + prefix_pages] = pt.expected_tags[src]
+    return PageTable(indptr.copy(), ind, exp, pt.page_tags, pt.num_pages, pt.stale_pages)

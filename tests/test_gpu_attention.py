@@ -123,6 +123,19 @@ def test_shared_pages_across_requests(orc):
     assert_close(got, case.oracle(orc, indices=ind), "shared pages")
 
 
+def test_shared_prefix_batch(orc):
+    """Eight requests whose first 40 pages are the same physical pages (a shared
+    2560-token prompt) on top of their own suffixes, FP8 and BF16."""
+    from fp8_paged_kv_decode_gb300 import workloads as W
+    for kv in ("fp8", "bf16"):
+        case = PagedCase(orc, 8, 32, 4, 64, [5000, 2700, 2561, 9000, 3333, 2600, 7000, 4096], kv=kv, seed=61)
+        pt = W.PageTable(case.indptr, case.indices, np.zeros(case.indices.size, np.uint32),
+                         np.zeros(case.P, np.uint32), case.P)
+        ind = W.share_prefix(pt, 40).indices
+        assert (ind[case.indptr[3]:case.indptr[3] + 40] == case.indices[:40]).all()
+        assert_close(bf16_out(case.gpu(indices=ind)), case.oracle(orc, indices=ind), "shared prefix " + kv)
+
+
 def test_empty_batch_is_noop():
     import torch
     import fp8_paged_kv_decode_gb300 as fkv

@@ -115,3 +115,17 @@ def test_admission_under_a_budget():
     budget = int(npg[:32].sum()) * 2 * pf
     assert W.admitted(2 * pf, npg, budget) == 32
     assert W.admitted(pf, npg, budget) > 32
+
+
+def test_share_prefix_rewrites_only_long_requests():
+    wl = W.WORKLOADS["tiny_gqa4"]
+    rng = np.random.default_rng(3)
+    pt = W.build_page_table(wl, np.array([100, 20, 64, 300]), rng)     # 7, 2, 4, 19 pages of 16 tokens
+    assert pt.indptr.tolist() == [0, 7, 9, 13, 32]
+    sp = W.share_prefix(pt, 3)
+    np.testing.assert_array_equal(sp.indices[:9], pt.indices[:9])      # request 0 itself; request 1 too short
+    np.testing.assert_array_equal(sp.indices[9:12], pt.indices[:3])    # request 2: first 3 pages shared
+    assert sp.indices[12] == pt.indices[12]
+    np.testing.assert_array_equal(sp.indices[13:16], pt.indices[:3])   # request 3
+    np.testing.assert_array_equal(sp.indices[16:], pt.indices[16:])
+    np.testing.assert_array_equal(sp.expected_tags[13:16], pt.expected_tags[:3])
