@@ -357,41 +357,85 @@ class Step:
         return res
 
     def timed_e2e(self, steps, warmup):
-        """The same step through host buffers: every step copies its inputs from
-        pinned host memory and reads the output and abort mask back."""
-        torch = self.torch
-        stream = torch.cuda.current_stream(self.device)
-        pin = lambda x: x.cpu().pin_memory()
-        h_in = [pin(x) for x in (self.q, self.k_new, self.v_new, self.slots_new, self.seq_lens, self.indptr,
-                                 self.indices, self.expected, self.page_tags)]
-        d_in = [self.q, self.k_new, self.v_new, self.slots_new, self.seq_lens, self.indptr, self.indices,
+        """The step through host buffers: every step copies all of its inputs
+        (queries, the new token's K/V and slot, seq_lens, the page table and
+        both tag arrays) from pinned host memory and reads the output and abort
+        mask back.  Inputs of a step are packed in one buffer (one copy each
+        way) and double-buffered on a copy stream, so step i+1's inputs and
+        step i-1's results move while step i computes."""
+        torch, fkv = self.torch, self.fkv
+        dev = self.device
+        srcs = [self.q, self.k_new, self.v_new, self.slots_new, self.seq_lens, self.indptr, self.indices,
                 self.expected, self.page_tags]
-        h_out = torch.empty_like(self.out, device="cpu").pin_memory()
-        h_mask = torch.empty_like(self.mask, device="cpu").pin_memory()
-        bi = sum(x.numel() * x.element_size() for x in h_in)
-        bo = h_out.numel() * h_out.element_size() + h_mask.numel() * h_mask.element_size()
+        offs, tot = [], 0
+        for x in srcs:
+            offs.append(tot)
+            tot += (x.numel() * x.element_size() + 255) // 256 * 256
+        out_bytes = self.out.numel() * self.out.element_size()
+        obytes = out_bytes + self.mask.numel()
+        d_in = [torch.empty(tot, dtype=torch.uint8, device=dev) for _ in range(2)]
+        h_in = [torch.empty(tot, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        d_out = [torch.empty(obytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+        h_out = [torch.empty(obytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
 
-        def one():
-            for h, d in zip(h_in, d_in):
-                d.copy_(h, non_blocking=True)
-            self.append()
-            self.check()
-            self.attend(True)
-            h_out.copy_(self.out, non_blocking=True)
-            h_mask.copy_(self.mask, non_blocking=True)
+        def views(buf):
+            v = []
+            for x, o in zip(srcs, offs):
+                n = x.numel() * x.element_size()
+                v.append(buf[o:o + n].view(x.dtype).view(x.shape))
+            return v
 
-        for _ in range(warmup):
-            one()
-        torch.cuda.synchronize(self.device)
+        for b in range(2):                       # the host holds the step's inputs
+            for hv, x in zip(views(h_in[b]), srcs):
+                hv.copy_(x.cpu())
+        dv = [views(d_in[b]) for b in range(2)]
+        ov = [(d_out[b][:out_bytes].view(torch.bfloat16).view(self.out.shape), d_out[b][out_bytes:]) for b in range(2)]
+        comp = torch.cuda.current_stream(dev)
+        cp = torch.cuda.Stream(dev)
+        h2d = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+
+        def step(i):
+            b = i & 1
+            q, kn, vn, sl, seq, indptr, ind, exp, tags = dv[b]
+            out, mask = ov[b]
+            comp.wait_event(h2d[b])
+            if self.fp8:
+                fkv.kv_append_fp8(kn, vn, sl, self.k_scale, self.v_scale, self.k_cache, self.v_cache)
+            else:
+                fkv.kv_append_bf16(kn, vn, sl, self.k_cache, self.v_cache)
+            fkv.kv_page_tag_check(tags, indptr, ind, exp, mask)
+            fkv.paged_decode_attn(q, self.k_cache, self.v_cache, indptr, ind, seq, self.sm, out, self.ws,
+                                  k_scale=self.k_scale if self.fp8 else None,
+                                  v_scale=self.v_scale if self.fp8 else None, abort_mask=mask)
+            done[b].record(comp)
+            with torch.cuda.stream(cp):
+                cp.wait_event(done[b])
+                h_out[b].copy_(d_out[b], non_blocking=True)      # this step's results
+                d_in[b].copy_(h_in[b], non_blocking=True)        # inputs of step i + 2
+                h2d[b].record(cp)
+
+        def run(n):
+            with torch.cuda.stream(cp):
+                for b in range(2):
+                    d_in[b].copy_(h_in[b], non_blocking=True)
+                    h2d[b].record(cp)
+            for i in range(n):
+                step(i)
+            cp.synchronize()
+
+        run(warmup)
+        torch.cuda.synchronize(dev)
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
-        t0.record(stream)
-        for _ in range(steps):
-            one()
-        t1.record(stream)
-        torch.cuda.synchronize(self.device)
+        t0.record(cp)
+        run(steps)
+        t1.record(cp)
+        torch.cuda.synchronize(dev)
         barrier()
-        return t0.elapsed_time(t1), bi, bo
+        last = (steps - 1) & 1                   # the host holds the last step's output
+        assert torch.equal(ov[last][0].view(torch.int16).reshape(-1).cpu(), h_out[last][:out_bytes].view(torch.int16))
+        return t0.elapsed_time(t1), tot, obytes
 
 
 class _Null:

@@ -56,7 +56,9 @@ class FkvError(RuntimeError):
 
 
 def library_path() -> str:
-    return os.path.join(_HERE, "libfkv.so")
+    """The in-tree libfkv.so (``FKV_LIBRARY_PATH`` points at another build,
+    e.g. a variant compiled with different options)."""
+    return os.environ.get("FKV_LIBRARY_PATH") or os.path.join(_HERE, "libfkv.so")
 
 
 def load_library():
