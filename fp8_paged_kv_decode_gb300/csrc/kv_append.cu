@@ -6,93 +6,143 @@
 // BF16, which halves its size.  One fp32 scale per KV head (per layer) maps
 // bf16 values into e4m3's range.
 //
-// Each thread handles 8 consecutive elements of one (token, kv head, K|V)
-// row: a 16-byte bf16 load, eight IEEE fp32 divisions, four
-// round-to-nearest-even saturating conversions, one 8-byte store.  Two warps'
-// worth of threads cover K and V of one (token, head); the pool layout is
-// [page][head][slot][128].  The work is tiny per decode step (one token per
-// request) and plain bandwidth for a bulk prefill write.
+// Grid: x over groups of 16 tokens, y over KV heads, so no thread divides a
+// 64-bit index.  16 threads serve one (token, head): 8 for its K row and 8
+// for its V row, 16 elements each (two 16-byte bf16 loads, one 16-byte e4m3
+// store).  The pool layout is [page][head][slot][128].  Per decode step the
+// work is tiny (one token per request); for a bulk prefill write it is plain
+// bandwidth, provided the arithmetic per element stays small -- hence the
+// division below.
 #include "fkv_common.cuh"
 
 namespace fkv {
 
 constexpr int kHeadDim = 128;
-constexpr int kChunks = kHeadDim / 8;     // 16-byte bf16 chunks per row
+constexpr int kElemsPerThread = 16;
+constexpr int kThreadsPerRow = kHeadDim / kElemsPerThread;   // 8
+constexpr int kThreadsPerToken = 2 * kThreadsPerRow;         // K and V: 16
+constexpr int kBlock = 256;
+constexpr int kTokensPerBlock = kBlock / kThreadsPerToken;   // 16
 
-__global__ void __launch_bounds__(256)
+// Division by the per-head scale, exactly as IEEE round-to-nearest fp32
+// division, from its correctly rounded reciprocal y = RN(1/b) and one
+// remainder correction (the correction step of Markstein's division,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", 1990):
+//     q0 = RN(a*y),  r = RN(a - b*q0) (one fma),  q = RN(q0 + r*y) (one fma).
+// The theorem's precondition (q0 within one ulp of a/b) does not hold for
+// every operand pair, so the claim rests on an exhaustive check instead: for
+// every bf16 significand of a and every fp32 significand of b, q equals the
+// correctly rounded quotient.  Powers of two carry over exactly while every
+// intermediate stays clear of underflow and overflow, which holds for
+// 2^-30 <= b <= 2^30 and 2^-64 <= |a| <= 2^64 (q0, q within 2^+-94, r zero or
+// at least 2^-111).  Below 2^-64, |a/b| < 2^-34 and both this and the exact
+// quotient give a zero code; such inputs only need a finite, correctly signed
+// result, which the sequence gives.  Anything else (a huge or non-finite a,
+// a scale out of range) takes __fdiv_rn.  The sequence runs on |a| and the
+// sign is put back afterwards, so -0 and tiny negatives keep their sign.
+__device__ __forceinline__ float div_by_recip(float a, float b, float y) {
+    const float m = fabsf(a);
+    const float q0 = __fmul_rn(m, y);
+    const float r = __fmaf_rn(-q0, b, m);
+    const float q = __fmaf_rn(r, y, q0);
+    return __uint_as_float(__float_as_uint(q) | (__float_as_uint(a) & 0x80000000u));
+}
+
+__device__ __forceinline__ bool recip_scale_ok(float b) {
+    return b >= 0x1p-30f && b <= 0x1p30f;     // false for NaN too
+}
+
+// Token of this thread (or -1: nothing to write) and the element offset of
+// its (slot, head) row in the pool; the thread's part of the row starts
+// chunk * 16 elements further on.
+__device__ __forceinline__ int64_t locate(const int64_t *__restrict__ slots, int64_t n_tokens, int32_t num_pages,
+                                          int32_t num_kv_heads, int32_t page_size, int32_t page_shift,
+                                          uint32_t *err, int64_t &offset_elems) {
+    const int64_t n = static_cast<int64_t>(blockIdx.x) * kTokensPerBlock + (threadIdx.x / kThreadsPerToken);
+    if (n >= n_tokens) return -1;
+    const int64_t slot = __ldg(slots + n);
+    if (slot < 0) return -1;                                      // padding token
+    const int64_t page = page_shift >= 0 ? (slot >> page_shift) : slot / page_size;
+    const int64_t off = slot - page * page_size;
+    if (page >= num_pages) {                                      // outside the pool: skip, record
+        if ((threadIdx.x % kThreadsPerToken) == 0) atomicOr(err, FKV_DEVERR_APPEND_SLOT);
+        return -1;
+    }
+    offset_elems = ((page * num_kv_heads + blockIdx.y) * page_size + off) * kHeadDim;
+    return n;
+}
+
+__global__ void __launch_bounds__(kBlock)
 kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                      const int64_t *__restrict__ slots, int64_t n_tokens,
                      const float *__restrict__ k_scale, const float *__restrict__ v_scale,
                      uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
-                     int32_t num_pages, int32_t num_kv_heads, int32_t page_size, uint32_t *err) {
+                     int32_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t page_shift,
+                     uint32_t *err) {
     grid_dep_wait();        // earlier readers of the pool (attention) have finished
     grid_dep_launch();
-    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t per_token = static_cast<int64_t>(num_kv_heads) * 2 * kChunks;
-    const int64_t n = gid / per_token;
-    if (n >= n_tokens) return;
-    const int rem = static_cast<int>(gid - n * per_token);
-    const int h = rem / (2 * kChunks);
-    const bool is_v = (rem / kChunks) & 1;
-    const int chunk = rem % kChunks;
-    const int64_t slot = __ldg(slots + n);
-    if (slot < 0) return;                          // padding token
-    const int64_t page = slot / page_size;
-    const int64_t off = slot - page * page_size;
-    if (page >= num_pages) {                       // outside the pool: skip, record
-        if (rem == 0) atomicOr(err, FKV_DEVERR_APPEND_SLOT);
-        return;
-    }
-    const int64_t row = n * num_kv_heads + h;
-    const uint4 raw = __ldg((is_v ? v_new : k_new) + row * kChunks + chunk);
-    const float scale = __ldg((is_v ? v_scale : k_scale) + h);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t packed[2];
+    int64_t dst_off = 0;
+    const int64_t n = locate(slots, n_tokens, num_pages, num_kv_heads, page_size, page_shift, err, dst_off);
+    if (n < 0) return;
+    const int h = blockIdx.y;
+    const int sub = threadIdx.x % kThreadsPerToken;
+    const bool is_v = sub >= kThreadsPerRow;
+    const int chunk = sub % kThreadsPerRow;
+    // 16 bf16 = two uint4 per thread; row (n, h) starts at uint4 index (n*Hkv + h) * 16
+    const uint4 *src = (is_v ? v_new : k_new) + (n * num_kv_heads + h) * (kHeadDim / 8) + chunk * 2;
+    const uint4 r0 = __ldg(src), r1 = __ldg(src + 1);
+    const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+    float x[kElemsPerThread];
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        float x[4];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const uint32_t u = w[2 * p + j];
-            x[2 * j] = __uint_as_float(u << 16);              // bf16 -> fp32, exact
-            x[2 * j + 1] = __uint_as_float(u & 0xFFFF0000u);
-        }
-        // one IEEE round-to-nearest division each, then one RNE to e4m3
-        const uint16_t c01 = f32x2_to_e4m3x2(__fdiv_rn(x[1], scale), __fdiv_rn(x[0], scale));
-        const uint16_t c23 = f32x2_to_e4m3x2(__fdiv_rn(x[3], scale), __fdiv_rn(x[2], scale));
-        packed[p] = static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
+    for (int j = 0; j < 8; ++j) {
+        x[2 * j] = __uint_as_float(w[j] << 16);                // bf16 -> fp32, exact
+        x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
     }
-    uint8_t *dst = (is_v ? v_cache : k_cache) +
-                   ((page * num_kv_heads + h) * page_size + off) * kHeadDim + chunk * 8;
-    *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+    const float b = __ldg((is_v ? v_scale : k_scale) + h);
+    uint32_t big = 0;                                          // largest |x| bit pattern
+#pragma unroll
+    for (int j = 0; j < 8; ++j) big = max(big, max(w[j] & 0x7FFF0000u, (w[j] << 16) & 0x7FFF0000u));
+    float q[kElemsPerThread];
+    if (recip_scale_ok(b) && big <= 0x5F800000u) {             // |x| <= 2^64 (finite)
+        const float y = __frcp_rn(b);
+#pragma unroll
+        for (int j = 0; j < kElemsPerThread; ++j) q[j] = div_by_recip(x[j], b, y);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kElemsPerThread; ++j) q[j] = __fdiv_rn(x[j], b);
+    }
+    uint32_t packed[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint16_t lo = f32x2_to_e4m3x2(q[4 * p + 1], q[4 * p]);
+        const uint16_t hi = f32x2_to_e4m3x2(q[4 * p + 3], q[4 * p + 2]);
+        packed[p] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+    uint8_t *dst = (is_v ? v_cache : k_cache) + dst_off + chunk * kElemsPerThread;
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
 }
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kBlock)
 kv_append_bf16_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                       const int64_t *__restrict__ slots, int64_t n_tokens,
                       uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
-                      int32_t num_pages, int32_t num_kv_heads, int32_t page_size, uint32_t *err) {
+                      int32_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t page_shift,
+                      uint32_t *err) {
     grid_dep_wait();        // earlier readers of the pool (attention) have finished
     grid_dep_launch();
-    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t per_token = static_cast<int64_t>(num_kv_heads) * 2 * kChunks;
-    const int64_t n = gid / per_token;
-    if (n >= n_tokens) return;
-    const int rem = static_cast<int>(gid - n * per_token);
-    const int h = rem / (2 * kChunks);
-    const bool is_v = (rem / kChunks) & 1;
-    const int chunk = rem % kChunks;
-    const int64_t slot = __ldg(slots + n);
-    if (slot < 0) return;
-    const int64_t page = slot / page_size;
-    const int64_t off = slot - page * page_size;
-    if (page >= num_pages) {
-        if (rem == 0) atomicOr(err, FKV_DEVERR_APPEND_SLOT);
-        return;
-    }
-    const int64_t row = n * num_kv_heads + h;
-    const uint4 raw = __ldg((is_v ? v_new : k_new) + row * kChunks + chunk);
-    (is_v ? v_cache : k_cache)[((page * num_kv_heads + h) * page_size + off) * kChunks + chunk] = raw;
+    int64_t dst_off = 0;
+    const int64_t n = locate(slots, n_tokens, num_pages, num_kv_heads, page_size, page_shift, err, dst_off);
+    if (n < 0) return;
+    const int h = blockIdx.y;
+    const int sub = threadIdx.x % kThreadsPerToken;
+    const bool is_v = sub >= kThreadsPerRow;
+    const int chunk = sub % kThreadsPerRow;
+    const uint4 *src = (is_v ? v_new : k_new) + (n * num_kv_heads + h) * (kHeadDim / 8) + chunk * 2;
+    const uint4 r0 = __ldg(src), r1 = __ldg(src + 1);
+    uint4 *dst = (is_v ? v_cache : k_cache) + dst_off / 8 + chunk * 2;
+    dst[0] = r0;
+    dst[1] = r1;
 }
 
 static fkv_status check_append_args(const void *k_new, const void *v_new, const int64_t *slot_mapping,
@@ -101,11 +151,25 @@ static fkv_status check_append_args(const void *k_new, const void *v_new, const 
                                     int32_t head_dim) {
     if (n_tokens < 0 || num_pages <= 0 || num_kv_heads <= 0 || page_size <= 0) return FKV_ERR_INVALID_ARG;
     if (head_dim != kHeadDim) return FKV_ERR_UNSUPPORTED;
+    if (num_kv_heads > 65535) return FKV_ERR_UNSUPPORTED;         // grid y
     if (n_tokens == 0) return FKV_OK;
     if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return FKV_ERR_INVALID_ARG;
     if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
         return FKV_ERR_INVALID_ARG;
     return FKV_OK;
+}
+
+// log2(page_size) when it is a power of two, else -1 (the kernel divides).
+static int32_t page_shift_of(int32_t page_size) {
+    if (page_size & (page_size - 1)) return -1;
+    int32_t s = 0;
+    while ((1 << s) < page_size) ++s;
+    return s;
+}
+
+static dim3 append_grid(int32_t n_tokens, int32_t num_kv_heads) {
+    return dim3(static_cast<unsigned>((n_tokens + kTokensPerBlock - 1) / kTokensPerBlock),
+                static_cast<unsigned>(num_kv_heads));
 }
 
 }  // namespace fkv
@@ -123,13 +187,11 @@ extern "C" fkv_status kv_append_fp8(const void *k_new, const void *v_new, const 
     if (!k_scale || !v_scale) return FKV_ERR_INVALID_ARG;
     uint32_t *err = device_error_word();
     if (!err) return FKV_ERR_CUDA;
-    const int64_t threads = static_cast<int64_t>(n_tokens) * num_kv_heads * 2 * kChunks;
-    const int64_t blocks = (threads + 255) / 256;
-    if (blocks > 0x7FFFFFFFLL) return FKV_ERR_INVALID_ARG;
-    const cudaError_t e = launch_pdl(kv_append_fp8_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+    const cudaError_t e = launch_pdl(kv_append_fp8_kernel, append_grid(n_tokens, num_kv_heads), dim3(kBlock), 0,
                                      static_cast<cudaStream_t>(stream), static_cast<const uint4 *>(k_new),
                                      static_cast<const uint4 *>(v_new), slot_mapping, static_cast<int64_t>(n_tokens),
-                                     k_scale, v_scale, k_cache, v_cache, num_pages, num_kv_heads, page_size, err);
+                                     k_scale, v_scale, k_cache, v_cache, num_pages, num_kv_heads, page_size,
+                                     page_shift_of(page_size), err);
     return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
 }
 
@@ -142,13 +204,10 @@ extern "C" fkv_status kv_append_bf16(const void *k_new, const void *v_new, const
     if (st != FKV_OK || n_tokens == 0) return st;
     uint32_t *err = device_error_word();
     if (!err) return FKV_ERR_CUDA;
-    const int64_t threads = static_cast<int64_t>(n_tokens) * num_kv_heads * 2 * kChunks;
-    const int64_t blocks = (threads + 255) / 256;
-    if (blocks > 0x7FFFFFFFLL) return FKV_ERR_INVALID_ARG;
-    const cudaError_t e = launch_pdl(kv_append_bf16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+    const cudaError_t e = launch_pdl(kv_append_bf16_kernel, append_grid(n_tokens, num_kv_heads), dim3(kBlock), 0,
                                      static_cast<cudaStream_t>(stream), static_cast<const uint4 *>(k_new),
                                      static_cast<const uint4 *>(v_new), slot_mapping, static_cast<int64_t>(n_tokens),
                                      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_pages,
-                                     num_kv_heads, page_size, err);
+                                     num_kv_heads, page_size, page_shift_of(page_size), err);
     return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
 }

@@ -75,6 +75,80 @@ def test_append_fp8_division_rounding(orc):
     assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
 
 
+def _midpoint_rows(orc, rng, H):
+    """Per KV head one (x, scale) pair with x/scale within two fp32 ulps of a
+    midpoint between neighbouring e4m3 values; the head's 128-element row holds
+    +-x * 2^j, j = -10..8, so each row lands near midpoints of several binades.
+    Returns rows [2][H][128] (K, V) and scales [2][H]."""
+    tab = orc.e4m3_decode_table()
+    c = rng.integers(0, 126, (2, H))
+    m = (tab[c] + tab[c + 1]) / 2
+    x = W.bits_to_f32(W.bf16_bits(rng.uniform(0.0625, 256, (2, H)).astype(np.float32)))
+    b0 = (x.astype(np.float64) / m).astype(np.float32)
+    nudge = np.arange(H) % 5 - 2
+    b = (b0.view(np.uint32).astype(np.int64) + nudge).astype(np.uint32).view(np.float32)
+    d = np.arange(128)
+    rows = (x[..., None] * np.exp2((d >> 1) % 19 - 10) * np.where(d & 1, -1.0, 1.0)).astype(np.float32)
+    return rows, b
+
+
+def test_append_fp8_division_near_midpoints(orc):
+    """The fast path's reciprocal-and-correction division decides codes exactly
+    where one fp32 ulp matters: quotients a few ulps from e4m3 midpoints."""
+    rng = np.random.default_rng(5)
+    H = 2048
+    rows, b = _midpoint_rows(orc, rng, H)
+    # the cases have teeth: an uncorrected quotient RN(|x| * RN(1/b)) flips codes
+    corr = (rows.astype(np.float64) / b[..., None]).astype(np.float32)
+    y = (1.0 / b.astype(np.float64)).astype(np.float32)
+    unc = (np.abs(rows) * y[..., None]).astype(np.float32) * np.sign(rows)
+    dif = corr != unc
+    assert (orc.e4m3_encode_array(corr[dif]) != orc.e4m3_encode_array(unc[dif])).sum() > 1000
+    kf, vf = rows[0][None], rows[1][None]                 # N = 1 token, H heads
+    gk, gv, kc, vc, _, _ = _run_fp8(orc, 1, H, 16, kf, vf, np.array([5]), b[0], b[1])
+    assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
+
+
+def test_append_fp8_division_fallback(orc):
+    """Scales outside [2^-30, 2^30] and rows holding huge or infinite values go
+    through IEEE division in the kernel; the codes are the same either way."""
+    rng = np.random.default_rng(6)
+    H = 16
+    rows, b = _midpoint_rows(orc, rng, H)
+    ks = b[0].copy()
+    ks[:6] = np.float32([2.0 ** -31, 2.0 ** 31, 1e-40, 2.0 ** -30, 2.0 ** 30, 3e-39])
+    kf = rows[0].copy()
+    kf[:6] *= np.float32(2.0 ** -40)                      # keep quotients in e4m3 range for tiny scales
+    kf[1] = rows[0][1] * np.float32(2.0 ** 40)
+    kf[4] = rows[0][4] * np.float32(2.0 ** 30)
+    vf = rows[1].copy()
+    vf[7, 3] = np.inf                                     # thread with an Inf: whole chunk on IEEE division
+    vf[8, 20] = np.float32(2.0 ** 65)                     # just above the fast path's limit
+    vf[9, 40] = -np.float32(2.0 ** 64)                    # at the limit: fast path
+    vf[10, 50] = np.float32(1e-42)                        # subnormal input
+    gk, gv, kc, vc, _, _ = _run_fp8(orc, 1, H, 16, kf[None], vf[None], np.array([9]), ks, b[1])
+    assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
+
+
+def test_append_fp8_all_bf16_patterns(orc):
+    """Every bf16 bit pattern under a spread of scales; NaN inputs give a NaN
+    code (either sign), everything else is bit-exact."""
+    rng = np.random.default_rng(7)
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(512, 1, 128)
+    H = 8
+    kb = np.repeat(pats, H, axis=1)
+    vb = kb[::-1].copy()
+    ks = np.float32([1.0, 1.0 / 448, 0.0137, 3.0, 2.0 ** -30, 2.0 ** 31, 7.5e-3, 1e-39])
+    vs = np.float32(rng.uniform(1e-3, 10, H))
+    kf, vf = W.bits_to_f32(kb), W.bits_to_f32(vb)
+    slots = np.arange(512, dtype=np.int64)
+    gk, gv, kc, vc, _, _ = _run_fp8(orc, 32, H, 16, kf, vf, slots, ks, vs)
+    for g, o, src in ((gk, kc, kf), (gv, vc, vf)):
+        nan = np.isnan(src).reshape(32, 16, H, 128).transpose(0, 2, 1, 3)
+        assert np.array_equal(g[~nan], o[~nan])
+        assert np.all((g[nan] & 0x7F) == 0x7F) and np.all((o[nan] & 0x7F) == 0x7F)
+
+
 def test_append_out_of_pool_slot_is_skipped_and_flagged(orc):
     import fp8_paged_kv_decode_gb300 as fkv
     fkv.device_error(clear=True)
