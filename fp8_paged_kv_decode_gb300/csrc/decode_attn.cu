@@ -106,12 +106,12 @@ struct AttnParams {
     const int64_t *prefix;     // [B+1] tile prefix over requests (tiles x Hkv)
     const int32_t *warp_req;   // [NW + 1] request holding each warp's first tile; [NW] = warps with work
     float *part_o;             // [slots][G][D]   slots = B*Hkv + NW
-    float2 *part_ml;           // [slots][G]  (m in log2 units, l; l < 0 marks an invalid unit)
+    float2 *part_ml;           // [slots][GP] (m in log2 units, l; l < 0 marks an invalid unit)
     int32_t *counters;         // [B*Hkv] arrivals per split unit (or per chunk of it)
     int32_t *chunk_counters;   // [slots] arrivals per first-level chunk, indexed by its first slot
     __nv_bfloat16 *out;
     uint32_t *err;
-    int B, Hq, Hkv, G, P, S, NW;
+    int B, Hq, Hkv, G, GP, P, S, NW;   // GP = G rounded up to even: 16-byte statistics rows
     float sm_scale_log2;
 };
 
@@ -268,7 +268,7 @@ __device__ void merge_parts(const AttnParams &p, int nw, int64_t slot0, int n, i
 #pragma unroll
             for (int hd = 0; hd < kMaxGroup; ++hd) {
                 if (hd >= G) break;
-                const float2 ml = __ldcg(p.part_ml + slot_of(k) * G + hd);
+                const float2 ml = __ldcg(p.part_ml + slot_of(k) * p.GP + hd);
                 bad |= ml.y < 0.f;
                 M[hd] = fmaxf(M[hd], ml.x);
             }
@@ -288,7 +288,7 @@ __device__ void merge_parts(const AttnParams &p, int nw, int64_t slot0, int n, i
 #pragma unroll
             for (int hd = 0; hd < kMaxGroup; ++hd) {
                 if (hd >= G) break;
-                const float2 ml = __ldcg(p.part_ml + slot_of(k) * G + hd);
+                const float2 ml = __ldcg(p.part_ml + slot_of(k) * p.GP + hd);
                 const float f = ex2(ml.x - M[hd]);
                 L[hd] += f * ml.y;
                 if (k0 == 0) F[hd] = f;
@@ -317,7 +317,7 @@ __device__ void merge_parts(const AttnParams &p, int nw, int64_t slot0, int n, i
                     if (j < 32) {
                         f = __shfl_sync(kFull, F[hd], j & 31);
                     } else if (live && hd < G) {         // entries past the first 32: reload
-                        const float2 ml = __ldcg(p.part_ml + slot_of(j) * G + hd);
+                        const float2 ml = __ldcg(p.part_ml + slot_of(j) * p.GP + hd);
                         f = ex2(ml.x - M[hd]);
                     }
                     fw[e][hd] = (live && hd < G) ? f : 0.f;
@@ -355,7 +355,106 @@ __device__ void merge_parts(const AttnParams &p, int nw, int64_t slot0, int n, i
         }
 #pragma unroll
         for (int hd = 0; hd < kMaxGroup; ++hd)
-            if (hd < G && lane == hd) __stcg(p.part_ml + dst * G + hd, make_float2(M[hd], bad ? -1.f : L[hd]));
+            if (hd < G && lane == hd) __stcg(p.part_ml + dst * p.GP + hd, make_float2(M[hd], bad ? -1.f : L[hd]));
+    }
+}
+
+// The same merge with the partials fetched into shared memory first, for a
+// warp whose stage ring is idle (the end of its range).  One round of 16-byte
+// cp.async copies brings the statistics and outputs of up to `cap` entries,
+// so the merge costs one memory round trip instead of one per pair of
+// entries; longer lists go in batches with a running rescale.
+__device__ void merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, int nw, int64_t slot0, int n,
+                                 int stride, bool maybe_empty, int64_t wk0, int64_t T, bool final_out, int r, int h,
+                                 float vsc, int64_t dst) {
+    const int lane = threadIdx.x;
+    const int G = p.G, GP = p.GP;
+    const uint32_t obytes = static_cast<uint32_t>(G) * kD * 4;     // one entry's outputs
+    const uint32_t mbytes = static_cast<uint32_t>(GP) * 8;         // one entry's statistics
+    const uint32_t mbase = sbuf + static_cast<uint32_t>(cap) * obytes;
+    auto empty = [&](int j) {
+        return maybe_empty && warp_lo(wk0 + j, T, nw) == warp_lo(wk0 + j + 1, T, nw);
+    };
+    auto slot_of = [&](int j) { return slot0 + static_cast<int64_t>(j) * stride; };
+    float M[kMaxGroup], L[kMaxGroup];
+    float4 acc[kMaxGroup];
+#pragma unroll
+    for (int hd = 0; hd < kMaxGroup; ++hd) {
+        M[hd] = -INFINITY;
+        L[hd] = 0.f;
+        acc[hd] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    bool bad = false;
+    for (int b0 = 0; b0 < n; b0 += cap) {
+        const int nb = min(cap, n - b0);
+        for (int e = 0; e < nb; ++e) {
+            if (empty(b0 + e)) continue;
+            const char *go = reinterpret_cast<const char *>(p.part_o + slot_of(b0 + e) * G * kD);
+            for (uint32_t c = lane * 16u; c < obytes; c += 512u) cp_async_16(sbuf + e * obytes + c, go + c);
+            const char *gm = reinterpret_cast<const char *>(p.part_ml + slot_of(b0 + e) * GP);
+            if (lane * 16u < mbytes) cp_async_16(mbase + e * mbytes + lane * 16u, gm + lane * 16u);
+        }
+        cp_async_wait_all();
+        __syncwarp();
+        float Mb[kMaxGroup];
+#pragma unroll
+        for (int hd = 0; hd < kMaxGroup; ++hd) Mb[hd] = M[hd];
+        for (int e = 0; e < nb; ++e) {
+            if (empty(b0 + e)) continue;
+#pragma unroll
+            for (int hd = 0; hd < kMaxGroup; ++hd) {
+                if (hd >= G) break;
+                const float2 ml = ld_shared_f2(mbase + e * mbytes + hd * 8);
+                bad |= ml.y < 0.f;
+                Mb[hd] = fmaxf(Mb[hd], ml.x);
+            }
+        }
+#pragma unroll
+        for (int hd = 0; hd < kMaxGroup; ++hd) {
+            const float f = M[hd] == -INFINITY ? 0.f : ex2(M[hd] - Mb[hd]);
+            L[hd] *= f;
+            acc[hd].x *= f;
+            acc[hd].y *= f;
+            acc[hd].z *= f;
+            acc[hd].w *= f;
+            M[hd] = Mb[hd];
+        }
+        for (int e = 0; e < nb; ++e) {
+            if (empty(b0 + e)) continue;
+#pragma unroll
+            for (int hd = 0; hd < kMaxGroup; ++hd) {
+                if (hd >= G) break;
+                const float2 ml = ld_shared_f2(mbase + e * mbytes + hd * 8);
+                const float wgt = ex2(ml.x - M[hd]);
+                L[hd] += wgt * ml.y;
+                const float4 v = ld_shared_f4(sbuf + e * obytes + hd * (kD * 4) + lane * 16);
+                acc[hd].x += wgt * v.x;
+                acc[hd].y += wgt * v.y;
+                acc[hd].z += wgt * v.z;
+                acc[hd].w += wgt * v.w;
+            }
+        }
+        __syncwarp();                                      // the next batch reuses the buffer
+    }
+    if (final_out) {
+#pragma unroll
+        for (int hd = 0; hd < kMaxGroup; ++hd) {
+            if (hd >= G) break;
+            const float sc = bad ? 0.f : vsc / L[hd];
+            uint2 *orow =
+                reinterpret_cast<uint2 *>(p.out + (static_cast<int64_t>(r) * p.Hq + h * G + hd) * kD) + lane;
+            *orow = make_uint2(pack_bf16x2(acc[hd].x * sc, acc[hd].y * sc),
+                               pack_bf16x2(acc[hd].z * sc, acc[hd].w * sc));
+        }
+    } else {
+#pragma unroll
+        for (int hd = 0; hd < kMaxGroup; ++hd) {
+            if (hd >= G) break;
+            __stcg(reinterpret_cast<float4 *>(p.part_o + (dst * G + hd) * kD) + lane, acc[hd]);
+        }
+#pragma unroll
+        for (int hd = 0; hd < kMaxGroup; ++hd)
+            if (hd < G && lane == hd) __stcg(p.part_ml + dst * GP + hd, make_float2(M[hd], bad ? -1.f : L[hd]));
     }
 }
 
@@ -401,6 +500,8 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
         return;
     }
     const int64_t n_tiles = hi - lo;
+    // entries one shared-memory merge round holds (the idle stage ring)
+    const int merge_cap = (NST * Lay::kStageBytes) / (G * kD * 4 + ((G + 1) & ~1) * 8);
 #if FKV_KV_EVICT_FIRST
     const uint64_t policy = l2_policy_evict_first();
 #else
@@ -797,7 +898,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                     __stcg(reinterpret_cast<float4 *>(prow + d0 + 4), make_float4(v[4], v[5], v[6], v[7]));
                     __stcg(reinterpret_cast<float4 *>(prow + d1), make_float4(v[8], v[9], v[10], v[11]));
                     __stcg(reinterpret_cast<float4 *>(prow + d1 + 4), make_float4(v[12], v[13], v[14], v[15]));
-                    if (g == 0) __stcg(p.part_ml + slot * G + hd, make_float2(m[j], unit_bad ? -1.f : lt[j]));
+                    if (g == 0) __stcg(p.part_ml + slot * p.GP + hd, make_float2(m[j], unit_bad ? -1.f : lt[j]));
                 }
             }
             if (!whole) {
@@ -805,11 +906,21 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                 // merges.  Units split over more than kChunk warps merge in two
                 // levels (chunks of kChunk consecutive parts, then the chunks),
                 // so no single warp reads a long unit's partials serially.
+                // Arrivals are acquire-release atomics by lane 0 after a warp
+                // barrier: they publish this warp's partial and, for the last
+                // arriver, make every other part visible.  At the end of the
+                // range the stage ring is idle and the merge reads through it.
                 const int64_t s0 = p.prefix[C.r] + static_cast<int64_t>(C.h) * C.nt;
                 const int64_t wf = warp_of_tile(s0, T, nw), wl = warp_of_tile(s0 + C.nt - 1, T, nw);
                 const int span = static_cast<int>(wl - wf + 1);
                 const bool maybe_empty = T < nw;
-                __threadfence();
+                const bool ring_idle = i == n_tiles - 1;
+                auto merge = [&](int64_t sl0, int cnt, int stride, bool me, int64_t wk0, bool fin, int64_t d) {
+                    if (ring_idle)
+                        merge_parts_smem(p, sbase, merge_cap, nw, sl0, cnt, stride, me, wk0, T, fin, C.r, C.h, vsc, d);
+                    else
+                        merge_parts(p, nw, sl0, cnt, stride, me, wk0, T, fin, C.r, C.h, vsc, d);
+                };
                 __syncwarp();
                 if (maybe_empty || span <= kChunk) {
                     int nparts = span;
@@ -818,27 +929,26 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                         for (int64_t x = wf; x <= wl; ++x) nparts += warp_lo(x, T, nw) != warp_lo(x + 1, T, nw);
                     }
                     int last = 0;
-                    if (lane == 0) last = atomicAdd(p.counters + u, 1) == nparts - 1;
+                    if (lane == 0) last = atomic_add_acq_rel_gpu(p.counters + u, 1) == nparts - 1;
                     if (__shfl_sync(kFull, last, 0)) {
-                        __threadfence();
-                        merge_parts(p, nw, u + wf, span, 1, maybe_empty, wf, T, true, C.r, C.h, vsc, 0);
+                        __syncwarp();
+                        merge(u + wf, span, 1, maybe_empty, wf, true, 0);
                     }
                 } else {
                     const int c0 = (static_cast<int>(w - wf) / kChunk) * kChunk;
                     const int csz = min(kChunk, span - c0);
                     const int nch = (span + kChunk - 1) / kChunk;
                     int last = 0;
-                    if (lane == 0) last = atomicAdd(p.chunk_counters + (u + wf + c0), 1) == csz - 1;
+                    if (lane == 0) last = atomic_add_acq_rel_gpu(p.chunk_counters + (u + wf + c0), 1) == csz - 1;
                     if (__shfl_sync(kFull, last, 0)) {
-                        __threadfence();
-                        merge_parts(p, nw, u + wf + c0, csz, 1, false, wf + c0, T, false, C.r, C.h, vsc, u + wf + c0);
-                        __threadfence();
+                        __syncwarp();
+                        merge(u + wf + c0, csz, 1, false, wf + c0, false, u + wf + c0);
                         __syncwarp();
                         int last2 = 0;
-                        if (lane == 0) last2 = atomicAdd(p.counters + u, 1) == nch - 1;
+                        if (lane == 0) last2 = atomic_add_acq_rel_gpu(p.counters + u, 1) == nch - 1;
                         if (__shfl_sync(kFull, last2, 0)) {
-                            __threadfence();
-                            merge_parts(p, nw, u + wf, nch, kChunk, false, wf, T, true, C.r, C.h, vsc, 0);
+                            __syncwarp();
+                            merge(u + wf, nch, kChunk, false, wf, true, 0);
                         }
                     }
                 }
@@ -913,7 +1023,7 @@ WsLayout ws_layout(int B, int Hkv, int G, int NW) {
     L.warp_req = align256(L.prefix + sizeof(int64_t) * (static_cast<size_t>(B) + 1));
     L.counters = align256(L.warp_req + sizeof(int32_t) * (NW + 1));
     L.part_ml = align256(L.counters + sizeof(int32_t) * (units + slots));
-    L.part_o = align256(L.part_ml + sizeof(float2) * slots * G);
+    L.part_o = align256(L.part_ml + sizeof(float2) * slots * ((G + 1) & ~1));
     L.total = align256(L.part_o + sizeof(float) * slots * G * kD);
     return L;
 }
@@ -1006,6 +1116,7 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
     p.Hq = num_q_heads;
     p.Hkv = num_kv_heads;
     p.G = G;
+    p.GP = (G + 1) & ~1;
     p.P = num_pages;
     p.S = page_size;
     p.NW = NW;

@@ -24,6 +24,12 @@ constexpr int kThreadsPerToken = 2 * kThreadsPerRow;         // K and V: 16
 constexpr int kBlock = 256;
 constexpr int kTokensPerBlock = kBlock / kThreadsPerToken;   // 16
 
+// Resident blocks per SM the FP8 kernel is compiled for: each thread keeps
+// 32 bytes of loads in flight, so residency sets the bytes in flight per SM.
+#ifndef FKV_APPEND_MIN_BLOCKS
+#define FKV_APPEND_MIN_BLOCKS 8
+#endif
+
 // Division by the per-head scale, exactly as IEEE round-to-nearest fp32
 // division, from its correctly rounded reciprocal y = RN(1/b) and one
 // remainder correction (the correction step of Markstein's division,
@@ -73,7 +79,7 @@ __device__ __forceinline__ int64_t locate(const int64_t *__restrict__ slots, int
     return n;
 }
 
-__global__ void __launch_bounds__(kBlock)
+__global__ void __launch_bounds__(kBlock, FKV_APPEND_MIN_BLOCKS)
 kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                      const int64_t *__restrict__ slots, int64_t n_tokens,
                      const float *__restrict__ k_scale, const float *__restrict__ v_scale,
@@ -93,31 +99,33 @@ kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ 
     const uint4 *src = (is_v ? v_new : k_new) + (n * num_kv_heads + h) * (kHeadDim / 8) + chunk * 2;
     const uint4 r0 = __ldg(src), r1 = __ldg(src + 1);
     const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-    float x[kElemsPerThread];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        x[2 * j] = __uint_as_float(w[j] << 16);                // bf16 -> fp32, exact
-        x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-    }
     const float b = __ldg((is_v ? v_scale : k_scale) + h);
     uint32_t big = 0;                                          // largest |x| bit pattern
 #pragma unroll
     for (int j = 0; j < 8; ++j) big = max(big, max(w[j] & 0x7FFF0000u, (w[j] << 16) & 0x7FFF0000u));
-    float q[kElemsPerThread];
+    // word j holds elements 2j (low half) and 2j+1; packed word p holds codes 4p .. 4p+3
+    uint32_t packed[4];
     if (recip_scale_ok(b) && big <= 0x5F800000u) {             // |x| <= 2^64 (finite)
         const float y = __frcp_rn(b);
 #pragma unroll
-        for (int j = 0; j < kElemsPerThread; ++j) q[j] = div_by_recip(x[j], b, y);
+        for (int p = 0; p < 4; ++p) {
+            const uint32_t u0 = w[2 * p], u1 = w[2 * p + 1];
+            const uint16_t lo = f32x2_to_e4m3x2(div_by_recip(__uint_as_float(u0 & 0xFFFF0000u), b, y),
+                                                div_by_recip(__uint_as_float(u0 << 16), b, y));
+            const uint16_t hi = f32x2_to_e4m3x2(div_by_recip(__uint_as_float(u1 & 0xFFFF0000u), b, y),
+                                                div_by_recip(__uint_as_float(u1 << 16), b, y));
+            packed[p] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        }
     } else {
 #pragma unroll
-        for (int j = 0; j < kElemsPerThread; ++j) q[j] = __fdiv_rn(x[j], b);
-    }
-    uint32_t packed[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const uint16_t lo = f32x2_to_e4m3x2(q[4 * p + 1], q[4 * p]);
-        const uint16_t hi = f32x2_to_e4m3x2(q[4 * p + 3], q[4 * p + 2]);
-        packed[p] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        for (int p = 0; p < 4; ++p) {
+            const uint32_t u0 = w[2 * p], u1 = w[2 * p + 1];
+            const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(u0 & 0xFFFF0000u), b),
+                                                __fdiv_rn(__uint_as_float(u0 << 16), b));
+            const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(u1 & 0xFFFF0000u), b),
+                                                __fdiv_rn(__uint_as_float(u1 << 16), b));
+            packed[p] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        }
     }
     uint8_t *dst = (is_v ? v_cache : k_cache) + dst_off + chunk * kElemsPerThread;
     *reinterpret_cast<uint4 *>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
