@@ -67,6 +67,7 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kChunk = 6;                // parts merged per first-level merge of a long unit
 constexpr int kMinTilesPerWarp = 8;      // small batches use fewer, longer warp ranges
+constexpr int kLocalPlanMax = 1024;      // batches up to this size: each warp finds its own range
 
 template <bool kFp8>
 struct Cfg;
@@ -103,6 +104,8 @@ struct AttnParams {
     const int32_t *indptr;
     const int32_t *indices;
     const int32_t *seq_lens;
+    const uint8_t *abort_mask; // nullptr: no request aborted
+    int64_t nnz;               // entries of page_indices
     const int64_t *prefix;     // [B+1] tile prefix over requests (tiles x Hkv)
     const int32_t *warp_req;   // [NW + 1] request holding each warp's first tile; [NW] = warps with work
     float *part_o;             // [slots][G][D]   slots = B*Hkv + NW
@@ -118,6 +121,42 @@ struct AttnParams {
 // ---------------------------------------------------------------------------
 // 1. plan
 // ---------------------------------------------------------------------------
+// Tiles of request r over all its KV heads; 0 if it is aborted, empty or has a
+// malformed page-table row (indptr out of order or past nnz, or fewer pages
+// than its length needs).  The plan kernel and the attention warps' own
+// schedule both count with this, so their prefixes agree exactly.  Loads go
+// to L2 (the inputs may have been written by the kernels just before).
+struct RequestInfo {
+    int64_t tiles;        // over all KV heads
+    int32_t seq_len, row; // length and first page-table entry
+};
+
+__device__ __forceinline__ RequestInfo request_info(const int32_t *seq_lens, const int32_t *indptr,
+                                                   const uint8_t *abort_mask, int64_t nnz, int r, int Hkv, int S,
+                                                   int tile) {
+    const int32_t sl = __ldcg(seq_lens + r);
+    const int32_t b = __ldcg(indptr + r), e = __ldcg(indptr + r + 1);
+    const bool alive = abort_mask == nullptr || __ldcg(abort_mask + r) == 0;
+    RequestInfo ri{0, sl, b};
+    if (alive && sl > 0 && b >= 0 && e >= b && e <= nnz && static_cast<int64_t>(e - b) * S >= sl)
+        ri.tiles = ((static_cast<int64_t>(sl) + tile - 1) / tile) * Hkv;
+    return ri;
+}
+
+__device__ __forceinline__ int64_t request_tiles(const int32_t *seq_lens, const int32_t *indptr,
+                                                 const uint8_t *abort_mask, int64_t nnz, int r, int Hkv, int S,
+                                                 int tile) {
+    return request_info(seq_lens, indptr, abort_mask, nnz, r, Hkv, S, tile).tiles;
+}
+
+// Warps that get work: every one streams at least kMinTilesPerWarp tiles, so a
+// small batch is not split into ranges too short to pay for their start-up
+// and merge (large batches use all NW).
+__device__ __forceinline__ int working_warps(int64_t T, int NW) {
+    const int64_t nw64 = (T + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
+    return static_cast<int>(nw64 < 1 ? 1 : (nw64 > NW ? NW : nw64));
+}
+
 __global__ void __launch_bounds__(kPlanThreads)
 attn_plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ indptr,
                  const uint8_t *__restrict__ abort_mask, int64_t nnz, int B, int Hkv, int S, int tile, int NW,
@@ -132,14 +171,7 @@ attn_plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict
     int64_t carry = 0;
     for (int base = 0; base < B; base += kPlanThreads) {
         const int r = base + tid;
-        int64_t cnt = 0;
-        if (r < B) {
-            const int64_t sl = seq_lens[r];
-            const int64_t b = indptr[r], e = indptr[r + 1];
-            const bool alive = abort_mask == nullptr || abort_mask[r] == 0;
-            if (alive && sl > 0 && b >= 0 && e >= b && e <= nnz && (e - b) * S >= sl)
-                cnt = ((sl + tile - 1) / tile) * Hkv;
-        }
+        const int64_t cnt = r < B ? request_tiles(seq_lens, indptr, abort_mask, nnz, r, Hkv, S, tile) : 0;
         int64_t x = cnt;                                   // inclusive warp scan
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -173,11 +205,7 @@ attn_plan_kernel(const int32_t *__restrict__ seq_lens, const int32_t *__restrict
     __syncthreads();
     const int64_t T = carry;
     const bool in_smem = B <= kPlanSmemPrefix;
-    // Warps that get work: every one streams at least kMinTilesPerWarp tiles,
-    // so a small batch is not split into ranges too short to pay for their
-    // start-up and merge (large batches use all NW).
-    int64_t nw64 = (T + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
-    const int nw = static_cast<int>(nw64 < 1 ? 1 : (nw64 > NW ? NW : nw64));
+    const int nw = working_warps(T, NW);
     if (tid == 0) warp_req[NW] = nw;
     for (int w = tid; w < nw; w += kPlanThreads) {
         const int64_t lo = static_cast<int64_t>(w) * T / nw;
@@ -222,6 +250,60 @@ __device__ __forceinline__ void cursor_next(Cursor &c, const AttnParams &p) {
     while (r < p.B && p.prefix[r + 1] == p.prefix[r]) ++r;      // requests with no tiles
     c.r = r;
     c.nt = r < p.B ? static_cast<int>((p.prefix[r + 1] - p.prefix[r]) / p.Hkv) : 0;
+}
+
+// cursor at tile x of request r, whose tiles start at `base` (nt per KV head)
+__device__ __forceinline__ void cursor_at(Cursor &c, int r, int64_t base, int nt, int64_t x) {
+    const int64_t rel = x - base;
+    c.r = r;
+    c.nt = nt;
+    c.h = static_cast<int>(rel / nt);
+    c.tt = static_cast<int>(rel - static_cast<int64_t>(c.h) * nt);
+}
+
+// Total tiles of the batch, computed by one warp from the inputs (the same
+// sum the plan kernel forms).
+__device__ __forceinline__ int64_t batch_tiles(const AttnParams &p, int tile) {
+    int64_t sum = 0;
+    for (int r = threadIdx.x; r < p.B; r += 32)
+        sum += request_tiles(p.seq_lens, p.indptr, p.abort_mask, p.nnz, r, p.Hkv, p.S, tile);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+    return sum;
+}
+
+// The request holding tile x (its index, first tile, tiles per KV head,
+// length and first page-table entry), by one warp scanning the batch: the
+// request a with prefix[a] <= x < prefix[a + 1], as the plan kernel's search
+// finds it.
+__device__ __forceinline__ void find_request(const AttnParams &p, int tile, int64_t x, int &r0, int64_t &base0,
+                                             int &nt0, int &sl0, int &row0) {
+    const int lane = threadIdx.x;
+    int64_t carry = 0;
+    r0 = -1;
+    for (int b = 0; b < p.B && r0 < 0; b += 32) {
+        const int r = b + lane;
+        RequestInfo ri{0, 0, 0};
+        if (r < p.B) ri = request_info(p.seq_lens, p.indptr, p.abort_mask, p.nnz, r, p.Hkv, p.S, tile);
+        const int64_t cnt = ri.tiles;
+        int64_t inc = cnt;                                 // inclusive scan over the 32 requests
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o) inc += y;
+        }
+        const int64_t excl = carry + inc - cnt;
+        const unsigned hit = __ballot_sync(kFull, cnt > 0 && excl <= x && x < excl + cnt);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            r0 = b + src;
+            base0 = __shfl_sync(kFull, excl, src);
+            nt0 = static_cast<int>(__shfl_sync(kFull, cnt, src) / p.Hkv);
+            sl0 = __shfl_sync(kFull, ri.seq_len, src);
+            row0 = __shfl_sync(kFull, ri.row, src);
+        }
+        carry += __shfl_sync(kFull, inc, 31);
+    }
 }
 
 __device__ __forceinline__ uint32_t lo16(uint32_t x) { return x & 0xFFFFu; }
@@ -483,19 +565,44 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
         prefetch_tensormap(&tmV);
     }
     __syncwarp();
-    grid_dep_wait();                                   // plan results are visible
 
-    const int64_t T = p.prefix[p.B];
-    const int nw = p.warp_req[p.NW];                   // warps with work (<= NW)
+    // Schedule.  A batch of up to kLocalPlanMax requests is scheduled here,
+    // by every warp from the inputs, so the first copies go out without
+    // waiting for the plan kernel; the plan kernel triggers this grid only
+    // after its own grid_dep_wait, so every kernel before it in the stream
+    // has completed and the inputs are final.  The plan's outputs (prefix
+    // table, zeroed arrival counters) are read only after wait_plan().
+    bool planned = false;
+    auto wait_plan = [&]() {
+        if (!planned) {
+            grid_dep_wait();
+            planned = true;
+        }
+    };
     // rows of requests with no tiles (aborted, empty, malformed) are zero
-    for (int r = w; r < p.B; r += p.NW) {
-        if (p.prefix[r + 1] != p.prefix[r]) continue;
-        uint4 *orow = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(r) * p.Hq * kD);
-        for (int c = lane; c < p.Hq * kD / 8; c += 32) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+    auto zero_rows = [&]() {
+        for (int r = w; r < p.B; r += p.NW) {
+            if (p.prefix[r + 1] != p.prefix[r]) continue;
+            uint4 *orow = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(r) * p.Hq * kD);
+            for (int c = lane; c < p.Hq * kD / 8; c += 32) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    const bool local = p.B <= kLocalPlanMax;
+    int64_t T;
+    int nw;
+    if (local) {
+        T = batch_tiles(p, kTile);
+        nw = working_warps(T, p.NW);
+    } else {
+        wait_plan();
+        T = p.prefix[p.B];
+        nw = p.warp_req[p.NW];                         // warps with work (<= NW)
     }
     const int64_t lo = w < nw ? warp_lo(w, T, nw) : 0;
     const int64_t hi = w < nw ? warp_lo(w + 1, T, nw) : 0;
     if (lo >= hi) {
+        wait_plan();
+        zero_rows();
         grid_dep_launch();
         return;
     }
@@ -509,15 +616,28 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
 #endif
 
     // ---------------- load side ----------------
-    Cursor L;
-    cursor_init(L, p, lo, p.warp_req[w]);
+    Cursor L, C;
     int pid_r = -1, pbase = 0, pidA = -1, pidB = -1, lseq = 0, lneed = 0;
     int64_t lrow0 = 0;
+    if (local) {
+        int r0, nt0, sl0, row0;
+        int64_t base0;
+        find_request(p, kTile, lo, r0, base0, nt0, sl0, row0);
+        cursor_at(L, r0, base0, nt0, lo);
+        pid_r = r0;                                    // the first request's page-table row is known
+        lseq = sl0;
+        lrow0 = row0;
+        lneed = (lseq + S - 1) / S;
+        pbase = -1000;
+    } else {
+        cursor_init(L, p, lo, p.warp_req[w]);
+    }
+    C = L;
     uint32_t bad_bits = 0;                             // bit s: stage s has an out-of-pool page
 
     auto fetch_ids = [&](int b) -> int {
         const int pos = b + lane;
-        return pos < lneed ? __ldg(p.indices + lrow0 + pos) : -1;
+        return pos < lneed ? __ldcg(p.indices + lrow0 + pos) : -1;
     };
     auto page_id = [&](int pos) -> int {
         if (pos < pbase || pos >= pbase + 64) {
@@ -534,8 +654,8 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     auto issue = [&](int stage) {
         if (L.r != pid_r) {
             pid_r = L.r;
-            lseq = __ldg(p.seq_lens + L.r);
-            lrow0 = __ldg(p.indptr + L.r);
+            lseq = __ldcg(p.seq_lens + L.r);
+            lrow0 = __ldcg(p.indptr + L.r);
             lneed = (lseq + S - 1) / S;
             pbase = -1000;
         }
@@ -579,12 +699,13 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     const int n_pro = n_tiles < NST ? static_cast<int>(n_tiles) : NST;
     for (int i = 0; i < n_pro; ++i) {
         issue(i);
+        if (L.tt + 1 >= L.nt && L.h + 1 >= Hkv) wait_plan();   // next tile: another request (prefix table)
         cursor_next(L, p);
     }
+    wait_plan();
+    zero_rows();
 
     // ---------------- compute side ----------------
-    Cursor C;
-    cursor_init(C, p, lo, p.warp_req[w]);
     uint32_t qb[8][2];
     float cfac[2] = {0.f, 0.f};
     float m[2], l[2];
@@ -1104,6 +1225,8 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
     p.indptr = page_indptr;
     p.indices = page_indices;
     p.seq_lens = seq_lens;
+    p.abort_mask = abort_mask;
+    p.nnz = nnz;
     p.prefix = reinterpret_cast<const int64_t *>(ws + wl.prefix);
     p.warp_req = reinterpret_cast<const int32_t *>(ws + wl.warp_req);
     p.counters = reinterpret_cast<int32_t *>(ws + wl.counters);

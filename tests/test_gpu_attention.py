@@ -189,3 +189,17 @@ def test_graph_captured_step_equals_eager(orc):
     torch.cuda.synchronize()
     assert int(mask.sum()) > 0
     assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+@pytest.mark.parametrize("B,kv", [(1024, "fp8"), (1025, "fp8"), (1025, "bf16"), (2000, "fp8")])
+def test_large_batches_both_schedules(orc, B, kv):
+    """Up to 1024 requests every attention warp finds its own range from the
+    inputs; larger batches read the plan kernel's prefix table.  Both agree
+    with the oracle, with empty, aborted and ragged requests mixed in."""
+    rng = np.random.default_rng(B + (kv == "bf16"))
+    seq = rng.integers(0, 90, B)
+    seq[rng.choice(B, 20, replace=False)] = 0
+    case = PagedCase(orc, B, 8, 2, 16, seq, kv=kv, seed=B)
+    abort = (rng.random(B) < 0.05).astype(np.uint8)
+    got = bf16_out(case.gpu(abort_mask=abort))
+    assert_close(got, case.oracle(orc, abort_mask=abort), "B=%d kv=%s" % (B, kv))
