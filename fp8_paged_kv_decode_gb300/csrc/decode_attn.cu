@@ -51,6 +51,10 @@
 #ifndef FKV_BF16_STAGES
 #define FKV_BF16_STAGES 2
 #endif
+// How the producer warp waits for a stage to be released.
+#ifndef FKV_PRODUCER_WAIT
+#define FKV_PRODUCER_WAIT mbar_wait_bounded_sleep
+#endif
 // L2 hint of the K/V tile copies (streamed once unless pages are shared).
 #ifndef FKV_KV_EVICT_FIRST
 #define FKV_KV_EVICT_FIRST 1
@@ -67,7 +71,10 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kChunk = 6;                // parts merged per first-level merge of a long unit
 constexpr int kMinTilesPerWarp = 8;      // small batches use fewer, longer warp ranges
-constexpr int kLocalPlanMax = 1024;      // batches up to this size: each warp finds its own range
+constexpr int kLocalPlanMax = 1024;
+// Attention CTA: one warp that both issues copies and computes, or (kWS) a
+// producer warp that issues copies and a consumer warp that computes.
+__host__ __device__ constexpr int attn_threads(bool ws) { return ws ? 64 : 32; }      // batches up to this size: each warp finds its own range
 
 template <bool kFp8>
 struct Cfg;
@@ -92,7 +99,8 @@ struct Layout {
     static constexpr int kHalfBytes = kTile * 128;              // one column block of a K (or V) tile
     static constexpr int kTileBytes = kHalves * kHalfBytes;     // a K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;          // K then V
-    static constexpr int kSmem = 1024 + kStages * kStageBytes + 8 * kStages;
+    // stage buffers, then per stage a full and an empty mbarrier and a bad-page flag
+    static constexpr int kSmem = 1024 + kStages * kStageBytes + 20 * kStages;
     static_assert(kTile == 32 || kTile == 64, "tile of 32 or 64 tokens");
     static_assert(kHalfBytes % 1024 == 0, "stage buffers stay 1024-byte aligned for the 128B swizzle");
 };
@@ -265,7 +273,7 @@ __device__ __forceinline__ void cursor_at(Cursor &c, int r, int64_t base, int nt
 // sum the plan kernel forms).
 __device__ __forceinline__ int64_t batch_tiles(const AttnParams &p, int tile) {
     int64_t sum = 0;
-    for (int r = threadIdx.x; r < p.B; r += 32)
+    for (int r = threadIdx.x & 31; r < p.B; r += 32)
         sum += request_tiles(p.seq_lens, p.indptr, p.abort_mask, p.nnz, r, p.Hkv, p.S, tile);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
@@ -278,7 +286,7 @@ __device__ __forceinline__ int64_t batch_tiles(const AttnParams &p, int tile) {
 // finds it.
 __device__ __forceinline__ void find_request(const AttnParams &p, int tile, int64_t x, int &r0, int64_t &base0,
                                              int &nt0, int &sl0, int &row0) {
-    const int lane = threadIdx.x;
+    const int lane = threadIdx.x & 31;
     int64_t carry = 0;
     r0 = -1;
     for (int b = 0; b < p.B && r0 < 0; b += 32) {
@@ -330,7 +338,7 @@ __device__ __forceinline__ int64_t warp_of_tile(int64_t x, int64_t T, int NW) {
 // 4 dims per lane) in flight.
 __device__ void merge_parts(const AttnParams &p, int nw, int64_t slot0, int n, int stride, bool maybe_empty,
                             int64_t wk0, int64_t T, bool final_out, int r, int h, float vsc, int64_t dst) {
-    const int lane = threadIdx.x;
+    const int lane = threadIdx.x & 31;
     const int G = p.G;
     auto empty = [&](int j) {
         return maybe_empty && warp_lo(wk0 + j, T, nw) == warp_lo(wk0 + j + 1, T, nw);
@@ -449,7 +457,7 @@ __device__ void merge_parts(const AttnParams &p, int nw, int64_t slot0, int n, i
 __device__ void merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, int nw, int64_t slot0, int n,
                                  int stride, bool maybe_empty, int64_t wk0, int64_t T, bool final_out, int r, int h,
                                  float vsc, int64_t dst) {
-    const int lane = threadIdx.x;
+    const int lane = threadIdx.x & 31;
     const int G = p.G, GP = p.GP;
     const uint32_t obytes = static_cast<uint32_t>(G) * kD * 4;     // one entry's outputs
     const uint32_t mbytes = static_cast<uint32_t>(GP) * 8;         // one entry's statistics
@@ -540,8 +548,8 @@ __device__ void merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, in
     }
 }
 
-template <bool kFp8>
-__global__ void __launch_bounds__(32, 1)
+template <bool kFp8, bool kWS>
+__global__ void __launch_bounds__(attn_threads(kWS), 1)
 paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV) {
     using Lay = Layout<kFp8>;
@@ -552,19 +560,32 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t bars = sbase + NST * Lay::kStageBytes;
-    const int lane = threadIdx.x;
+    // Stage s completes on full[s] when its copies land.  With kWS the CTA has
+    // two warps: warp 0 issues the K/V copies (the producer) and warp 1
+    // computes (the consumer), which releases a stage on empty[s].  A tensor
+    // copy takes ~80 ns to issue, so moving the issue off the computing warp
+    // pays when a 64-token tile spans several small pages (2 to 8 copies per
+    // stage); with one page per tile (2 copies) the single warp, refilling a
+    // stage right after it is consumed, is ~2 % faster.
+    const uint32_t full_bars = sbase + NST * Lay::kStageBytes;
+    const uint32_t empty_bars = full_bars + 8 * NST;
+    const uint32_t bad_flags = empty_bars + 8 * NST;      // per stage: 1 = a page id outside the pool
+    const int lane = threadIdx.x & 31;
+    const bool producer = kWS && threadIdx.x < 32;
     const int g = lane >> 2, t = lane & 3;
     const int w = blockIdx.x;
     const int S = p.S, Hkv = p.Hkv, G = p.G;
 
-    if (lane == 0) {
-        for (int s = 0; s < NST; ++s) mbar_init(bars + 8 * s, 1);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(full_bars + 8 * s, 1);
+            mbar_init(empty_bars + 8 * s, 1);
+        }
         fence_mbar_init();
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
-    __syncwarp();
+    __syncthreads();
 
     // Schedule.  A batch of up to kLocalPlanMax requests is scheduled here,
     // by every warp from the inputs, so the first copies go out without
@@ -601,8 +622,10 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     const int64_t lo = w < nw ? warp_lo(w, T, nw) : 0;
     const int64_t hi = w < nw ? warp_lo(w + 1, T, nw) : 0;
     if (lo >= hi) {
-        wait_plan();
-        zero_rows();
+        if (!producer) {
+            wait_plan();
+            zero_rows();
+        }
         grid_dep_launch();
         return;
     }
@@ -633,7 +656,6 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
         cursor_init(L, p, lo, p.warp_req[w]);
     }
     C = L;
-    uint32_t bad_bits = 0;                             // bit s: stage s has an out-of-pool page
 
     auto fetch_ids = [&](int b) -> int {
         const int pos = b + lane;
@@ -678,9 +700,9 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             ids[k] = id;
             bytes += 2u * rows * 128u * Lay::kHalves;
         }
-        bad_bits = (bad_bits & ~(1u << stage)) | (static_cast<uint32_t>(bad) << stage);
         if (lane == 0) {
-            const uint32_t bar = bars + 8 * stage;
+            const uint32_t bar = full_bars + 8 * stage;
+            st_shared_u32(bad_flags + 4 * stage, bad ? 1u : 0u);   // published by the arrive below
             mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -696,11 +718,32 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
         }
     };
 
-    const int n_pro = n_tiles < NST ? static_cast<int>(n_tiles) : NST;
-    for (int i = 0; i < n_pro; ++i) {
-        issue(i);
-        if (L.tt + 1 >= L.nt && L.h + 1 >= Hkv) wait_plan();   // next tile: another request (prefix table)
-        cursor_next(L, p);
+    if (!kWS) {                                        // fill the ring
+        const int n_pro = n_tiles < NST ? static_cast<int>(n_tiles) : NST;
+        for (int i = 0; i < n_pro; ++i) {
+            issue(i);
+            if (L.tt + 1 >= L.nt && L.h + 1 >= Hkv) wait_plan();   // next tile: another request (prefix table)
+            cursor_next(L, p);
+        }
+    }
+    if (producer) {
+        // Stream the range: stage s is refilled once the consumer has released
+        // it (tile j waits for the release of tile j - NST).
+        for (int64_t j = 0; j < n_tiles; ++j) {
+            const int st = static_cast<int>(j % NST);
+            if (j >= NST && !FKV_PRODUCER_WAIT(empty_bars + 8 * st, static_cast<uint32_t>((j / NST - 1) & 1),
+                                               kWaitLimitNs)) {
+                if (lane == 0) atomicOr(p.err, FKV_DEVERR_TIMEOUT);
+                break;                                 // the consumer gives up on the copies never issued
+            }
+            issue(st);
+            if (j + 1 < n_tiles) {
+                if (L.tt + 1 >= L.nt && L.h + 1 >= Hkv) wait_plan();   // next tile: another request (prefix table)
+                cursor_next(L, p);
+            }
+        }
+        grid_dep_launch();
+        return;
     }
     wait_plan();
     zero_rows();
@@ -781,16 +824,17 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
         }
 
         // ---- wait for this stage's copies ----
-        if (!mbar_wait_bounded(bars + 8 * s, parity, kWaitLimitNs)) {
+        if (!mbar_wait_bounded(full_bars + 8 * s, parity, kWaitLimitNs)) {
             if (lane == 0) atomicOr(p.err, FKV_DEVERR_TIMEOUT);
             // wind down: let every copy still in flight land before leaving
+            // (the producer is never more than NST tiles ahead)
             const int64_t last = i + NST < n_tiles ? i + NST : n_tiles;
             for (int64_t j = i; j < last; ++j)
-                (void)mbar_wait_bounded(bars + 8 * static_cast<int>(j % NST),
+                (void)mbar_wait_bounded(full_bars + 8 * static_cast<int>(j % NST),
                                         static_cast<uint32_t>((j / NST) & 1), kDrainLimitNs);
             return;
         }
-        if ((bad_bits >> s) & 1u) {
+        if (ld_shared_u32(bad_flags + 4 * s)) {
             if (!unit_bad && lane == 0) atomicOr(p.err, FKV_DEVERR_ATTN_PAGE);
             unit_bad = true;
         }
@@ -967,8 +1011,11 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
         }
         __syncwarp();
 
-        // ---- refill this stage with the tile NST ahead ----
-        if (i + NST < n_tiles) {
+        if (kWS) {
+            // ---- hand the stage back to the producer ----
+            if (lane == 0) mbar_arrive(empty_bars + 8 * s);
+        } else if (i + NST < n_tiles) {
+            // ---- refill this stage with the tile NST ahead ----
             issue(s);
             cursor_next(L, p);
         }
@@ -1087,7 +1134,7 @@ namespace {
 
 constexpr int kMaxDev = 64;
 std::mutex g_mu;
-int g_ctas_per_sm[kMaxDev][2];       // [dev][kv_fp8]
+int g_ctas_per_sm[kMaxDev][2][2];    // [dev][kv_fp8][ws]
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1103,20 +1150,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kWS>
 int ctas_per_sm() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
     std::lock_guard<std::mutex> lk(g_mu);
-    int &v = g_ctas_per_sm[dev][kFp8 ? 1 : 0];
+    int &v = g_ctas_per_sm[dev][kFp8 ? 1 : 0][kWS ? 1 : 0];
     if (!v) {
         const int smem = Layout<kFp8>::kSmem;
-        if (cudaFuncSetAttribute(paged_decode_attn_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(paged_decode_attn_kernel<kFp8, kWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem) != cudaSuccess)
             return 0;
         int nb = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, paged_decode_attn_kernel<kFp8>, 32, smem) !=
-                cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, paged_decode_attn_kernel<kFp8, kWS>,
+                                                          attn_threads(kWS), smem) != cudaSuccess ||
             nb <= 0)
             return 0;
         v = nb < 16 ? nb : 16;
@@ -1124,10 +1171,17 @@ int ctas_per_sm() {
     return v;
 }
 
-int grid_warps(bool fp8) {
+// Computing warps of one launch (one per CTA).
+int grid_warps(bool fp8, bool ws) {
     const int sms = device_sm_count();
-    const int per = fp8 ? ctas_per_sm<true>() : ctas_per_sm<false>();
+    const int per = fp8 ? (ws ? ctas_per_sm<true, true>() : ctas_per_sm<true, false>())
+                        : (ws ? ctas_per_sm<false, true>() : ctas_per_sm<false, false>());
     return sms * per;
+}
+
+// The two-warp CTA when a tile spans several pages.
+bool use_ws(int page_size, bool fp8) {
+    return page_size < (fp8 ? Layout<true>::kTile : Layout<false>::kTile);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -1177,8 +1231,11 @@ extern "C" size_t paged_decode_attn_workspace_size(int32_t batch, int32_t num_q_
     if (head_dim != kD || (kv_dtype != FKV_KV_FP8_E4M3 && kv_dtype != FKV_KV_BF16)) return 0;
     const int G = num_q_heads / num_kv_heads;
     if (G > kMaxGroup) return 0;
-    const int NW = grid_warps(kv_dtype == FKV_KV_FP8_E4M3);
-    if (NW <= 0) return 0;
+    // sized for either CTA shape (the page size is not known here)
+    const bool fp8 = kv_dtype == FKV_KV_FP8_E4M3;
+    const int n1 = grid_warps(fp8, false), n2 = grid_warps(fp8, true);
+    const int NW = n1 > n2 ? n1 : n2;
+    if (n1 <= 0 || n2 <= 0) return 0;
     return ws_layout(batch, num_kv_heads, G, NW).total;
 }
 
@@ -1205,7 +1262,8 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return FKV_ERR_INVALID_ARG;
-    const int NW = grid_warps(fp8);
+    const bool two_warp = use_ws(page_size, fp8);
+    const int NW = grid_warps(fp8, two_warp);
     uint32_t *err = device_error_word();
     if (NW <= 0 || !err) return FKV_ERR_CUDA;
     const WsLayout wl = ws_layout(batch, num_kv_heads, G, NW);
@@ -1251,10 +1309,15 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
                                reinterpret_cast<int64_t *>(ws + wl.prefix), reinterpret_cast<int32_t *>(ws + wl.warp_req),
                                reinterpret_cast<int32_t *>(ws + wl.counters));
     if (e != cudaSuccess) return FKV_ERR_CUDA;
-    if (fp8)
-        e = launch_pdl(paged_decode_attn_kernel<true>, dim3(NW), dim3(32), Layout<true>::kSmem, st, p, tmK, tmV);
+    const dim3 grid(NW), block(attn_threads(two_warp));
+    if (fp8 && two_warp)
+        e = launch_pdl(paged_decode_attn_kernel<true, true>, grid, block, Layout<true>::kSmem, st, p, tmK, tmV);
+    else if (fp8)
+        e = launch_pdl(paged_decode_attn_kernel<true, false>, grid, block, Layout<true>::kSmem, st, p, tmK, tmV);
+    else if (two_warp)
+        e = launch_pdl(paged_decode_attn_kernel<false, true>, grid, block, Layout<false>::kSmem, st, p, tmK, tmV);
     else
-        e = launch_pdl(paged_decode_attn_kernel<false>, dim3(NW), dim3(32), Layout<false>::kSmem, st, p, tmK, tmV);
+        e = launch_pdl(paged_decode_attn_kernel<false, false>, grid, block, Layout<false>::kSmem, st, p, tmK, tmV);
     if (e != cudaSuccess) return FKV_ERR_CUDA;
     return FKV_OK;
 }
