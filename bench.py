@@ -21,6 +21,7 @@ collective on the data path; timing is max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -50,6 +51,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--kv", default="fp8", choices=["fp8", "bf16"], help="KV cache dtype of the main line")
+    ap.add_argument("--page-size", type=int, default=None, help="override the workload's page size (tokens)")
+    ap.add_argument("--stale-frac", type=float, default=None,
+                    help="override the workload's fraction of stale (reallocated) pages, e.g. 0 for a clean batch")
     ap.add_argument("--skip-extras", action="store_true", help="only the FP8 headline and e2e")
     ap.add_argument("--cpu-requests", type=int, default=4, help="requests in the oracle's bounded sample")
     ap.add_argument("--shared-prefix", action="store_true",
@@ -67,6 +71,17 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def selected_workload(W, args):
+    """The --workload entry, with --page-size and --stale-frac applied when given."""
+    wl = W.WORKLOADS[args.workload]
+    if args.page_size is not None and args.page_size != wl.page_size:
+        wl = dataclasses.replace(wl, name="%s (page %d)" % (wl.name, args.page_size), page_size=args.page_size)
+    if args.stale_frac is not None and args.stale_frac != wl.stale_frac:
+        wl = dataclasses.replace(wl, name="%s (stale_frac=%g)" % (wl.name, args.stale_frac),
+                                 stale_frac=args.stale_frac)
+    return wl
 
 
 def peak_hbm():
@@ -527,7 +542,7 @@ def run_reference(args):
     import oracle
     from fp8_paged_kv_decode_gb300 import workloads as W
     orc = oracle.default()
-    wl = W.WORKLOADS[args.workload]
+    wl = selected_workload(W, args)
     device = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
     db = W.device_batch(wl, device, seed=wl.seed)
     n_req = min(4, wl.batch)
@@ -676,7 +691,7 @@ def main():
     barrier()
     fkv.load_library()
 
-    wl = W.WORKLOADS[args.workload]
+    wl = selected_workload(W, args)
     db = W.device_batch(wl, device, seed=wl.seed + rank)
     fp8 = Step(db, args.kv, device)
     fkv.device_error(clear=True)
