@@ -69,8 +69,14 @@ constexpr int kPlanSmemPrefix = 4096;    // requests whose prefix the plan searc
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // a copy that has not landed in 2 s has failed
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr uint32_t kFull = 0xffffffffu;
-constexpr int kChunk = 6;                // parts merged per first-level merge of a long unit
-constexpr int kMinTilesPerWarp = 8;      // small batches use fewer, longer warp ranges
+#ifndef FKV_MERGE_CHUNK
+#define FKV_MERGE_CHUNK 6
+#endif
+#ifndef FKV_MIN_TILES_PER_WARP
+#define FKV_MIN_TILES_PER_WARP 8
+#endif
+constexpr int kChunk = FKV_MERGE_CHUNK;  // parts merged per first-level merge of a long unit
+constexpr int kMinTilesPerWarp = FKV_MIN_TILES_PER_WARP;   // small batches use fewer, longer warp ranges
 constexpr int kLocalPlanMax = 1024;
 // Attention CTA: one warp that both issues copies and computes, or (kWS) a
 // producer warp that issues copies and a consumer warp that computes.
@@ -1106,11 +1112,15 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                     const int c0 = (static_cast<int>(w - wf) / kChunk) * kChunk;
                     const int csz = min(kChunk, span - c0);
                     const int nch = (span + kChunk - 1) / kChunk;
-                    int last = 0;
-                    if (lane == 0) last = atomic_add_acq_rel_gpu(p.chunk_counters + (u + wf + c0), 1) == csz - 1;
+                    // A one-part chunk (the unit's last warp, whose part ends early in
+                    // its range) is already its own result: it skips the first
+                    // level instead of merging itself mid-range.
+                    int last = csz == 1;
+                    if (csz > 1 && lane == 0)
+                        last = atomic_add_acq_rel_gpu(p.chunk_counters + (u + wf + c0), 1) == csz - 1;
                     if (__shfl_sync(kFull, last, 0)) {
                         __syncwarp();
-                        merge(u + wf + c0, csz, 1, false, wf + c0, false, u + wf + c0);
+                        if (csz > 1) merge(u + wf + c0, csz, 1, false, wf + c0, false, u + wf + c0);
                         __syncwarp();
                         int last2 = 0;
                         if (lane == 0) last2 = atomic_add_acq_rel_gpu(p.counters + u, 1) == nch - 1;

@@ -203,3 +203,13 @@ def test_large_batches_both_schedules(orc, B, kv):
     abort = (rng.random(B) < 0.05).astype(np.uint8)
     got = bf16_out(case.gpu(abort_mask=abort))
     assert_close(got, case.oracle(orc, abort_mask=abort), "B=%d kv=%s" % (B, kv))
+
+
+@pytest.mark.parametrize("kv", ["fp8", "bf16"])
+@pytest.mark.parametrize("Hkv,seq", [(1, [3584]), (2, [3584]), (1, [3585]), (1, [25 * 512])])
+def test_long_unit_merge_chunks(orc, kv, Hkv, seq):
+    """One long unit split over several warps (8 tiles each): 3584 tokens are
+    56 tiles over 7 warps, so the second merge chunk holds only the unit's
+    last warp; the others give trailing chunks of other sizes."""
+    case = PagedCase(orc, 1, 8 * Hkv, Hkv, 64, seq, kv=kv, seed=sum(seq) + Hkv)
+    assert_close(bf16_out(case.gpu()), case.oracle(orc), "Hkv=%d seq=%s kv=%s" % (Hkv, seq, kv))
