@@ -286,38 +286,51 @@ __device__ __forceinline__ int64_t batch_tiles(const AttnParams &p, int tile) {
     return sum;
 }
 
-// The request holding tile x (its index, first tile, tiles per KV head,
-// length and first page-table entry), by one warp scanning the batch: the
-// request a with prefix[a] <= x < prefix[a + 1], as the plan kernel's search
-// finds it.
-__device__ __forceinline__ void find_request(const AttnParams &p, int tile, int64_t x, int &r0, int64_t &base0,
-                                             int &nt0, int &sl0, int &row0) {
+// Where the warp's first tile lies: the request r0 holding tile x (prefix[r0]
+// <= x < prefix[r0 + 1], as the plan kernel's search finds it), its first
+// tile, tiles per KV head, length and first page-table entry.
+struct FirstRequest {
+    int r0 = -1, nt0 = 0, sl0 = 0, row0 = 0;
+    int64_t base0 = 0;
+};
+
+// One step of the search: the 32 requests b .. b + 31 (this lane's is ri),
+// `carry` tiles before them.  Returns the tiles of these 32 requests.
+__device__ __forceinline__ int64_t scan_requests(const RequestInfo &ri, int b, int64_t carry, int64_t x, int Hkv,
+                                                 FirstRequest &fr) {
     const int lane = threadIdx.x & 31;
+    const int64_t cnt = ri.tiles;
+    int64_t inc = cnt;                                     // inclusive scan over the 32 requests
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += y;
+    }
+    const int64_t excl = carry + inc - cnt;
+    const unsigned hit = __ballot_sync(kFull, cnt > 0 && excl <= x && x < excl + cnt);
+    if (hit) {
+        const int src = __ffs(hit) - 1;
+        fr.r0 = b + src;
+        fr.base0 = __shfl_sync(kFull, excl, src);
+        fr.nt0 = static_cast<int>(__shfl_sync(kFull, cnt, src) / Hkv);
+        fr.sl0 = __shfl_sync(kFull, ri.seq_len, src);
+        fr.row0 = __shfl_sync(kFull, ri.row, src);
+    }
+    return __shfl_sync(kFull, inc, 31);
+}
+
+// The same search reading the requests 32 at a time (any batch size).
+__device__ __forceinline__ FirstRequest find_request(const AttnParams &p, int tile, int64_t x) {
+    const int lane = threadIdx.x & 31;
+    FirstRequest fr;
     int64_t carry = 0;
-    r0 = -1;
-    for (int b = 0; b < p.B && r0 < 0; b += 32) {
+    for (int b = 0; b < p.B && fr.r0 < 0; b += 32) {
         const int r = b + lane;
         RequestInfo ri{0, 0, 0};
         if (r < p.B) ri = request_info(p.seq_lens, p.indptr, p.abort_mask, p.nnz, r, p.Hkv, p.S, tile);
-        const int64_t cnt = ri.tiles;
-        int64_t inc = cnt;                                 // inclusive scan over the 32 requests
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int64_t y = __shfl_up_sync(kFull, inc, o);
-            if (lane >= o) inc += y;
-        }
-        const int64_t excl = carry + inc - cnt;
-        const unsigned hit = __ballot_sync(kFull, cnt > 0 && excl <= x && x < excl + cnt);
-        if (hit) {
-            const int src = __ffs(hit) - 1;
-            r0 = b + src;
-            base0 = __shfl_sync(kFull, excl, src);
-            nt0 = static_cast<int>(__shfl_sync(kFull, cnt, src) / p.Hkv);
-            sl0 = __shfl_sync(kFull, ri.seq_len, src);
-            row0 = __shfl_sync(kFull, ri.row, src);
-        }
-        carry += __shfl_sync(kFull, inc, 31);
+        carry += scan_requests(ri, b, carry, x, p.Hkv, fr);
     }
+    return fr;
 }
 
 __device__ __forceinline__ uint32_t lo16(uint32_t x) { return x & 0xFFFFu; }
@@ -617,7 +630,20 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     const bool local = p.B <= kLocalPlanMax;
     int64_t T;
     int nw;
-    if (local) {
+    // Up to 64 requests: one load of every request's row (two per lane) serves
+    // both the total and the search for the first request.
+    const bool cached = p.B <= 64;
+    RequestInfo rc[2] = {{0, 0, 0}, {0, 0, 0}};
+    if (cached) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+            if (32 * c + lane < p.B)
+                rc[c] = request_info(p.seq_lens, p.indptr, p.abort_mask, p.nnz, 32 * c + lane, Hkv, S, kTile);
+        T = rc[0].tiles + rc[1].tiles;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) T += __shfl_xor_sync(kFull, T, o);
+        nw = working_warps(T, p.NW);
+    } else if (local) {
         T = batch_tiles(p, kTile);
         nw = working_warps(T, p.NW);
     } else {
@@ -649,13 +675,17 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     int pid_r = -1, pbase = 0, pidA = -1, pidB = -1, lseq = 0, lneed = 0;
     int64_t lrow0 = 0;
     if (local) {
-        int r0, nt0, sl0, row0;
-        int64_t base0;
-        find_request(p, kTile, lo, r0, base0, nt0, sl0, row0);
-        cursor_at(L, r0, base0, nt0, lo);
-        pid_r = r0;                                    // the first request's page-table row is known
-        lseq = sl0;
-        lrow0 = row0;
+        FirstRequest fr;
+        if (cached) {
+            const int64_t c1 = scan_requests(rc[0], 0, 0, lo, Hkv, fr);
+            if (fr.r0 < 0) scan_requests(rc[1], 32, c1, lo, Hkv, fr);
+        } else {
+            fr = find_request(p, kTile, lo);
+        }
+        cursor_at(L, fr.r0, fr.base0, fr.nt0, lo);
+        pid_r = fr.r0;                                 // the first request's page-table row is known
+        lseq = fr.sl0;
+        lrow0 = fr.row0;
         lneed = (lseq + S - 1) / S;
         pbase = -1000;
     } else {
