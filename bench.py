@@ -93,11 +93,31 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+def code_tokens(text):
+    """Source text without // comments and with whitespace collapsed: edits
+    to comments leave the hash of the code unchanged."""
+    out = []
+    for line in text.splitlines():
+        i = line.find("//")
+        if i >= 0:
+            line = line[:i]
+        line = " ".join(line.split())
+        if line:
+            out.append(line)
+    return "\n".join(out)
+
+
+def kernel_source_hash(sources=None):
+    """Hash of the attention kernel's code (its two source files), which the
+    recorded ncu traffic figures are keyed to."""
     h = hashlib.sha256()
     for f in ("decode_attn.cu", "fkv_common.cuh"):
-        with open(os.path.join(ROOT, "fp8_paged_kv_decode_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        if sources is None:
+            with open(os.path.join(ROOT, "fp8_paged_kv_decode_gb300", "csrc", f)) as fh:
+                text = fh.read()
+        else:
+            text = sources[f]
+        h.update(code_tokens(text).encode())
     return h.hexdigest()[:16]
 
 

@@ -12,25 +12,29 @@
 //
 // GB300 design (two launches, chained with programmatic dependent launch):
 //  1. plan (one CTA): tiles per request from seq_lens / abort mask / page
-//     table; prefix over requests; the first request of each worker warp;
+//     table; prefix over requests; the first request of each computing warp;
 //     zeroed arrival counters.  A "tile" is kTile tokens of one
 //     (request, KV head) unit.
-//  2. attention (persistent, one warp per CTA, grid = SMs x resident CTAs):
-//     the concatenation of all units' tiles is cut into equal contiguous
-//     ranges, one per warp (split-KV with even load across the lognormal
-//     context mix).  Each warp streams its tiles through a private ring of
-//     shared-memory stages filled by 128B-swizzled TMA tensor copies (one 2-D
-//     box per page: the K and V tiles of a (page, head) are contiguous in HBM).
-//     QK^T and PV run on the tensor cores as m16n8k16 MMAs with tokens on M
-//     and the G <= 8 query heads of the KV head on N; e4m3 codes become f16
-//     exactly in registers (the per-head scales fold into the logit factor and
-//     the output); softmax is online in fp32 with warp shuffles.  A warp that
-//     covers a whole unit writes the bf16 output directly; otherwise it writes
-//     an unnormalised fp32 partial (o, m, l), and the last of the unit's warps
-//     to arrive (an atomic counter, no waiting) merges the partials with a
-//     log-sum-exp rescale (two levels for units split over many warps).  Rows
-//     of requests with no tiles (aborted, empty, malformed) are zero-filled by
-//     the warps, one request each.
+//  2. attention (persistent, one computing warp per CTA, grid = SMs x
+//     resident CTAs): the concatenation of all units' tiles is cut into equal
+//     contiguous ranges, one per computing warp (split-KV with even load
+//     across the lognormal context mix).  For batches of up to 1024 requests
+//     each warp finds its own range from the inputs and starts its copies
+//     before the plan kernel has finished.  Each warp streams its tiles
+//     through a private ring of shared-memory stages filled by 128B-swizzled
+//     TMA tensor copies (one box per page: the K and V tiles of a (page, head)
+//     are contiguous in HBM); when a tile spans several small pages a second,
+//     producer warp issues the copies.  QK^T and PV run on the tensor cores as
+//     m16n8k16 MMAs with tokens on M and the G <= 8 query heads of the KV head
+//     on N; e4m3 codes become f16 exactly in registers (the per-head scales
+//     fold into the logit factor and the output); softmax is online in fp32
+//     with warp shuffles.  A warp that covers a whole unit writes the bf16
+//     output directly; otherwise it writes an unnormalised fp32 partial
+//     (o, m, l), and the last of the unit's warps to arrive (an atomic
+//     counter, no waiting) merges the partials with a log-sum-exp rescale
+//     (two levels for units split over many warps), through its idle stage
+//     ring at the end of its range.  Rows of requests with no tiles (aborted,
+//     empty, malformed) are zero-filled by the warps, one request each.
 #include <cudaTypedefs.h>
 
 #include <cmath>
