@@ -1223,9 +1223,14 @@ int grid_warps(bool fp8, bool ws) {
     return sms * per;
 }
 
-// The two-warp CTA when a tile spans several pages.
+// The two-warp CTA when a tile spans several pages (page sizes below
+// FKV_WS_PAGE_LIMIT, by default the tile).
+#ifndef FKV_WS_PAGE_LIMIT
+#define FKV_WS_PAGE_LIMIT 64
+#endif
 bool use_ws(int page_size, bool fp8) {
-    return page_size < (fp8 ? Layout<true>::kTile : Layout<false>::kTile);
+    const int tile = fp8 ? Layout<true>::kTile : Layout<false>::kTile;
+    return page_size < (FKV_WS_PAGE_LIMIT < tile ? FKV_WS_PAGE_LIMIT : tile);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
