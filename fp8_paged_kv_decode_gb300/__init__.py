@@ -64,6 +64,9 @@ def library_path() -> str:
 def load_library():
     """Load libfkv.so (raises if it has not been built)."""
     global _lib
+    lib = _lib
+    if lib is not None:
+        return lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -104,14 +107,15 @@ def load_library():
 # marshalling helpers
 # ---------------------------------------------------------------------------
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # plain integers: the entry points' argtypes convert them to void *
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream):
     import torch
     if stream is None:
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def _need(cond, msg):
