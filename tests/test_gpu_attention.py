@@ -213,3 +213,14 @@ def test_long_unit_merge_chunks(orc, kv, Hkv, seq):
     last warp; the others give trailing chunks of other sizes."""
     case = PagedCase(orc, 1, 8 * Hkv, Hkv, 64, seq, kv=kv, seed=sum(seq) + Hkv)
     assert_close(bf16_out(case.gpu()), case.oracle(orc), "Hkv=%d seq=%s kv=%s" % (Hkv, seq, kv))
+
+
+def test_batch_beyond_plan_smem_table(orc):
+    """More requests than the plan kernel keeps in shared memory (4096): its
+    warp search reads the prefix table from global memory."""
+    rng = np.random.default_rng(4500)
+    B = 4500
+    seq = rng.integers(0, 40, B)
+    case = PagedCase(orc, B, 2, 1, 16, seq, kv="fp8", seed=4500)
+    abort = (rng.random(B) < 0.02).astype(np.uint8)
+    assert_close(bf16_out(case.gpu(abort_mask=abort)), case.oracle(orc, abort_mask=abort), "B=4500")
