@@ -45,18 +45,20 @@ def test_peaky_softmax(orc):
     assert_close(bf16_out(case.gpu()), case.oracle(orc), "peaky")
 
 
-def test_fail_closed_rows(orc):
+@pytest.mark.parametrize("S", [16, 64])
+def test_fail_closed_rows(orc, S):
     """Aborted, empty, over-long and bad-page requests give zero rows; the
     other rows still match; the bad page id is never dereferenced and is
-    reported in the device error word."""
+    reported in the device error word.  Page size 16 runs the producer-warp
+    CTA, 64 the single-warp one."""
     import fp8_paged_kv_decode_gb300 as fkv
     B = 6
-    case = PagedCase(orc, B, 16, 2, 16, [100, 200, 300, 400, 500, 600], seed=4)
+    case = PagedCase(orc, B, 16, 2, S, [100, 200, 300, 400, 500, 600], seed=4)
     seq = case.seq.copy()
     seq[1] = 0
-    seq[3] = 16 * ((400 + 15) // 16) + 1               # one token more than its pages hold
+    seq[3] = S * ((400 + S - 1) // S) + 1               # one token more than its pages hold
     ind = case.indices.copy()
-    ind[case.indptr[4] + 7] = case.P + 1000               # outside the pool
+    ind[case.indptr[4] + 3] = case.P + 1000               # outside the pool
     am = np.array([1, 0, 0, 0, 0, 0], np.uint8)
     fkv.device_error(clear=True)
     got = bf16_out(case.gpu(abort_mask=am, seq=seq, indices=ind))
@@ -76,12 +78,14 @@ def test_no_tracker_path_equals_all_clear_mask(orc):
     assert np.array_equal(a, b)
 
 
-def test_abort_equals_absent_bytewise(orc):
+@pytest.mark.parametrize("S", [64, 16])
+def test_abort_equals_absent_bytewise(orc, S):
     """Aborting a request leaves every other row byte-identical to a batch
-    without that request (the split plan depends only on the live requests)."""
+    without that request (the split plan depends only on the live requests),
+    for both CTA shapes."""
     import torch
     import fp8_paged_kv_decode_gb300 as fkv
-    case = PagedCase(orc, 5, 32, 4, 64, [9000, 300, 20000, 4000, 1], seed=6)
+    case = PagedCase(orc, 5, 32, 4, S, [9000, 300, 20000, 4000, 1], seed=6)
     am = np.array([0, 0, 1, 0, 0], np.uint8)
     full = case.gpu(abort_mask=am).cpu()
     keep = [0, 1, 3, 4]
