@@ -23,7 +23,10 @@ namespace fkv {
 constexpr int kCalThreads = 256;
 constexpr int kCalRows = kCalThreads / 16;    // token rows per CTA per iteration
 
-__global__ void __launch_bounds__(kCalThreads)
+constexpr int kCalUnroll = 4;                 // rows whose loads each thread keeps in flight
+constexpr int kCalBlocksPerSM = 8;            // resident CTAs per SM the kernel is compiled for
+
+__global__ void __launch_bounds__(kCalThreads, kCalBlocksPerSM)
 kv_amax_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v, int64_t n_tokens, int32_t num_kv_heads,
                uint32_t *__restrict__ k_amax, uint32_t *__restrict__ v_amax) {
     grid_dep_wait();
@@ -33,13 +36,22 @@ kv_amax_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v, int64_t
     const bool is_v = blockIdx.z != 0;
     const uint4 *src = is_v ? v : k;
     const int lane16 = threadIdx.x & 15;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kCalRows;
     uint32_t mx = 0;
-    for (int64_t n = static_cast<int64_t>(blockIdx.x) * kCalRows + (threadIdx.x >> 4); n < n_tokens;
-         n += static_cast<int64_t>(gridDim.x) * kCalRows) {
-        const uint4 x = __ldg(src + (n * num_kv_heads + h) * 16 + lane16);
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    for (int64_t n0 = static_cast<int64_t>(blockIdx.x) * kCalRows + (threadIdx.x >> 4); n0 < n_tokens;
+         n0 += kCalUnroll * stride) {
+        uint4 x[kCalUnroll];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+        for (int u = 0; u < kCalUnroll; ++u) {       // every load issued before any is used
+            const int64_t n = n0 + u * stride;
+            x[u] = n < n_tokens ? __ldg(src + (n * num_kv_heads + h) * 16 + lane16) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kCalUnroll; ++u) {
+            const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -81,7 +93,9 @@ extern "C" fkv_status kv_calibrate_scales(const void *k, const void *v, int64_t 
     if (n_tokens > 0) {
         const int sms = device_sm_count();
         int64_t gx = (n_tokens + kCalRows - 1) / kCalRows;
-        const int64_t target = std::max<int64_t>(1, static_cast<int64_t>(sms > 0 ? sms : 1) * 8 / (2 * num_kv_heads));
+        // one wave: kCalBlocksPerSM CTAs per SM over all (KV head, K|V) pairs
+        const int64_t target =
+            std::max<int64_t>(1, static_cast<int64_t>(sms > 0 ? sms : 1) * kCalBlocksPerSM / (2 * num_kv_heads));
         gx = std::min(gx, target);
         e = launch_pdl(kv_amax_kernel, dim3(static_cast<unsigned>(gx), num_kv_heads, 2), dim3(kCalThreads), 0, st,
                        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), n_tokens, num_kv_heads,
