@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--kv", default="fp8", choices=["fp8", "bf16"], help="KV cache dtype of the main line")
     ap.add_argument("--page-size", type=int, default=None, help="override the workload's page size (tokens)")
+    ap.add_argument("--ctx", default=None, help="override the workload's context lengths, e.g. fixed:16384")
     ap.add_argument("--stale-frac", type=float, default=None,
                     help="override the workload's fraction of stale (reallocated) pages, e.g. 0 for a clean batch")
     ap.add_argument("--skip-extras", action="store_true", help="only the FP8 headline and e2e")
@@ -74,8 +75,10 @@ def dist_env():
 
 
 def selected_workload(W, args):
-    """The --workload entry, with --page-size and --stale-frac applied when given."""
+    """The --workload entry, with --page-size, --ctx and --stale-frac applied when given."""
     wl = W.WORKLOADS[args.workload]
+    if args.ctx is not None and args.ctx != wl.ctx:
+        wl = dataclasses.replace(wl, name="%s (ctx %s)" % (wl.name, args.ctx), ctx=args.ctx)
     if args.page_size is not None and args.page_size != wl.page_size:
         wl = dataclasses.replace(wl, name="%s (page %d)" % (wl.name, args.page_size), page_size=args.page_size)
     if args.stale_frac is not None and args.stale_frac != wl.stale_frac:
@@ -121,9 +124,12 @@ def kernel_source_hash(sources=None):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kv):
+def recorded_traffic(kv, workload=HEADLINE):
     """DRAM bytes per paged_decode_attn call from a committed ncu summary, if it
-    was taken on the current kernel source (else None)."""
+    was taken on the current kernel source and on this workload (the figures
+    are for the headline batch; else None)."""
+    if workload != HEADLINE:
+        return None
     try:
         vals = {}
         with open(TRAFFIC_FILE) as f:
@@ -749,7 +755,7 @@ def main():
     attn_bytes, attended = fp8.attn_bytes()
     peak, peak_kind = peak_hbm()
     achieved = attn_bytes / (attn_ms / 1e3) / 1e9
-    traffic = recorded_traffic(args.kv)
+    traffic = recorded_traffic(args.kv, wl.name)
 
     e2e_steps = max(10, args.steps // 4)
     e2e_ms, bi, bo = fp8.timed_e2e(e2e_steps, max(3, args.warmup // 4))
@@ -789,7 +795,7 @@ def main():
         line["bf16_kv"] = {"value": world * wl.batch * max(10, args.steps // 2) / (bms / 1e3), "unit": "tokens/s",
                            "ms_per_step": bms / max(10, args.steps // 2), "attn_ms": battn, "attn_gbs": bach,
                            "frac": bach / peak, "algorithmic_bytes": bbytes,
-                           "traffic": (recorded_traffic("bf16") or {}).get("dram_bytes_per_call")}
+                           "traffic": (recorded_traffic("bf16", wl.name) or {}).get("dram_bytes_per_call")}
         line["fp8_over_bf16_attn_time"] = battn / attn_ms
         del bf
         torch.cuda.empty_cache()
