@@ -76,9 +76,15 @@ constexpr uint32_t kFull = 0xffffffffu;
 #ifndef FKV_MERGE_CHUNK
 #define FKV_MERGE_CHUNK 6
 #endif
+// Merges due in the middle of a warp's range wait for its end (1) or run at
+// once through registers (0).
+#ifndef FKV_DEFER_MIDRANGE
+#define FKV_DEFER_MIDRANGE 0
+#endif
 #ifndef FKV_MIN_TILES_PER_WARP
 #define FKV_MIN_TILES_PER_WARP 8
 #endif
+constexpr int kNone = 0, kFinalDue = 1, kChunkDue = 2;   // merge duties of a warp
 constexpr int kChunk = FKV_MERGE_CHUNK;  // parts merged per first-level merge of a long unit
 constexpr int kMinTilesPerWarp = FKV_MIN_TILES_PER_WARP;   // small batches use fewer, longer warp ranges
 constexpr int kLocalPlanMax = 1024;
@@ -109,8 +115,9 @@ struct Layout {
     static constexpr int kHalfBytes = kTile * 128;              // one column block of a K (or V) tile
     static constexpr int kTileBytes = kHalves * kHalfBytes;     // a K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;          // K then V
-    // stage buffers, then per stage a full and an empty mbarrier and a bad-page flag
-    static constexpr int kSmem = 1024 + kStages * kStageBytes + 20 * kStages;
+    // stage buffers, then per stage a full and an empty mbarrier, the merge
+    // mbarrier, and per stage a bad-page flag
+    static constexpr int kSmem = 1024 + kStages * kStageBytes + 20 * kStages + 8;
     static_assert(kTile == 32 || kTile == 64, "tile of 32 or 64 tokens");
     static_assert(kHalfBytes % 1024 == 0, "stage buffers stay 1024-byte aligned for the 128B swizzle");
 };
@@ -473,22 +480,25 @@ __device__ void merge_parts(const AttnParams &p, int nw, int64_t slot0, int n, i
 }
 
 // The same merge with the partials fetched into shared memory first, for a
-// warp whose stage ring is idle (the end of its range).  One round of 16-byte
-// cp.async copies brings the statistics and outputs of up to `cap` entries,
-// so the merge costs one memory round trip instead of one per pair of
-// entries; longer lists go in batches with a running rescale.
-__device__ void merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, int nw, int64_t slot0, int n,
-                                 int stride, bool maybe_empty, int64_t wk0, int64_t T, bool final_out, int r, int h,
-                                 float vsc, int64_t dst) {
+// warp whose stage ring is idle (the end of its range).  Each entry arrives in
+// two bulk copies (outputs, statistics) issued by the lane that owns it, all
+// completing on `bar`, so a batch of up to `cap` (<= 32) entries costs one
+// memory round trip.  The statistics are reduced across lanes (one entry per
+// lane); each entry's weights go to shared memory and the output pass reads
+// them back as broadcasts beside the entry's rows.  Longer lists go in batches
+// with a running rescale.  The caller has acquired every entry (an
+// acquire-release arrival after the writers' own); the proxy fence carries
+// that to the bulk copies.  Returns false if a batch's copies did not land in
+// time; nothing is written then.
+__device__ bool merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, uint32_t bar, uint32_t &phase, int nw,
+                                 int64_t slot0, int n, int stride, bool maybe_empty, int64_t wk0, int64_t T,
+                                 bool final_out, int r, int h, float vsc, int64_t dst) {
     const int lane = threadIdx.x & 31;
     const int G = p.G, GP = p.GP;
     const uint32_t obytes = static_cast<uint32_t>(G) * kD * 4;     // one entry's outputs
     const uint32_t mbytes = static_cast<uint32_t>(GP) * 8;         // one entry's statistics
     const uint32_t mbase = sbuf + static_cast<uint32_t>(cap) * obytes;
-    auto empty = [&](int j) {
-        return maybe_empty && warp_lo(wk0 + j, T, nw) == warp_lo(wk0 + j + 1, T, nw);
-    };
-    auto slot_of = [&](int j) { return slot0 + static_cast<int64_t>(j) * stride; };
+    const uint32_t wbase = mbase + static_cast<uint32_t>(cap) * mbytes;   // 8 weights per entry
     float M[kMaxGroup], L[kMaxGroup];
     float4 acc[kMaxGroup];
 #pragma unroll
@@ -500,64 +510,92 @@ __device__ void merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, in
     bool bad = false;
     for (int b0 = 0; b0 < n; b0 += cap) {
         const int nb = min(cap, n - b0);
-        for (int e = 0; e < nb; ++e) {
-            if (empty(b0 + e)) continue;
-            const char *go = reinterpret_cast<const char *>(p.part_o + slot_of(b0 + e) * G * kD);
-            for (uint32_t c = lane * 16u; c < obytes; c += 512u) cp_async_16(sbuf + e * obytes + c, go + c);
-            const char *gm = reinterpret_cast<const char *>(p.part_ml + slot_of(b0 + e) * GP);
-            if (lane * 16u < mbytes) cp_async_16(mbase + e * mbytes + lane * 16u, gm + lane * 16u);
-        }
-        cp_async_wait_all();
+        const int j = b0 + lane;
+        const bool live = lane < nb && !(maybe_empty && warp_lo(wk0 + j, T, nw) == warp_lo(wk0 + j + 1, T, nw));
+        const uint32_t lmask = __ballot_sync(kFull, live);
+        const int nv = __popc(lmask);
+        if (nv == 0) continue;
+        const uint32_t pos = __popc(lmask & ((1u << lane) - 1u));   // live entries are packed
+        if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nv) * (obytes + mbytes));
         __syncwarp();
-        float Mb[kMaxGroup];
-#pragma unroll
-        for (int hd = 0; hd < kMaxGroup; ++hd) Mb[hd] = M[hd];
-        for (int e = 0; e < nb; ++e) {
-            if (empty(b0 + e)) continue;
-#pragma unroll
-            for (int hd = 0; hd < kMaxGroup; ++hd) {
-                if (hd >= G) break;
-                const float2 ml = ld_shared_f2(mbase + e * mbytes + hd * 8);
-                bad |= ml.y < 0.f;
-                Mb[hd] = fmaxf(Mb[hd], ml.x);
-            }
+        if (live) {
+            const int64_t slot = slot0 + static_cast<int64_t>(j) * stride;
+            fence_proxy_async_global();
+            bulk_load(sbuf + pos * obytes, p.part_o + slot * G * kD, obytes, bar);
+            bulk_load(mbase + pos * mbytes, p.part_ml + slot * GP, mbytes, bar);
         }
+        if (!mbar_wait_bounded(bar, phase, kWaitLimitNs)) {
+            (void)mbar_wait_bounded(bar, phase, kDrainLimitNs);   // let copies in flight land
+            return false;
+        }
+        phase ^= 1u;
+        // statistics: lane e holds entry e
+        float mv[kMaxGroup], lv[kMaxGroup], wv[kMaxGroup];
 #pragma unroll
         for (int hd = 0; hd < kMaxGroup; ++hd) {
-            const float f = M[hd] == -INFINITY ? 0.f : ex2(M[hd] - Mb[hd]);
-            L[hd] *= f;
+            mv[hd] = -INFINITY;
+            lv[hd] = 0.f;
+            wv[hd] = 0.f;
+            if (hd < G && lane < nv) {
+                const float2 ml = ld_shared_f2(mbase + lane * mbytes + hd * 8);
+                mv[hd] = ml.x;
+                lv[hd] = ml.y;
+                bad |= ml.y < 0.f;
+            }
+        }
+        // all kMaxGroup heads, so the shuffle chains interleave (heads >= G
+        // carry m = -inf and weight 0 throughout)
+#pragma unroll
+        for (int hd = 0; hd < kMaxGroup; ++hd) {
+            float mb = mv[hd];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
+            mb = fmaxf(mb, M[hd]);
+            const float f = M[hd] == -INFINITY ? 0.f : ex2(M[hd] - mb);
+            wv[hd] = mv[hd] == -INFINITY ? 0.f : ex2(mv[hd] - mb);
+            float sl = wv[hd] * lv[hd];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) sl += __shfl_xor_sync(kFull, sl, o);
+            L[hd] = L[hd] * f + sl;
             acc[hd].x *= f;
             acc[hd].y *= f;
             acc[hd].z *= f;
             acc[hd].w *= f;
-            M[hd] = Mb[hd];
+            M[hd] = mb;
         }
-        for (int e = 0; e < nb; ++e) {
-            if (empty(b0 + e)) continue;
+        if (lane < nv) {
+            st_shared_f4(wbase + lane * 32, make_float4(wv[0], wv[1], wv[2], wv[3]));
+            st_shared_f4(wbase + lane * 32 + 16, make_float4(wv[4], wv[5], wv[6], wv[7]));
+        }
+        __syncwarp();
+        // outputs: 4 dims of every head per lane
+        for (int e = 0; e < nv; ++e) {
+            const float4 w0 = ld_shared_f4(wbase + e * 32), w1 = ld_shared_f4(wbase + e * 32 + 16);
+            const float wgt[kMaxGroup] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
             for (int hd = 0; hd < kMaxGroup; ++hd) {
-                if (hd >= G) break;
-                const float2 ml = ld_shared_f2(mbase + e * mbytes + hd * 8);
-                const float wgt = ex2(ml.x - M[hd]);
-                L[hd] += wgt * ml.y;
-                const float4 v = ld_shared_f4(sbuf + e * obytes + hd * (kD * 4) + lane * 16);
-                acc[hd].x += wgt * v.x;
-                acc[hd].y += wgt * v.y;
-                acc[hd].z += wgt * v.z;
-                acc[hd].w += wgt * v.w;
+                if (hd < G) {
+                    const float4 v = ld_shared_f4(sbuf + e * obytes + hd * (kD * 4) + lane * 16);
+                    acc[hd].x += wgt[hd] * v.x;
+                    acc[hd].y += wgt[hd] * v.y;
+                    acc[hd].z += wgt[hd] * v.z;
+                    acc[hd].w += wgt[hd] * v.w;
+                }
             }
         }
         __syncwarp();                                      // the next batch reuses the buffer
     }
+    bad = __any_sync(kFull, bad);
     if (final_out) {
 #pragma unroll
         for (int hd = 0; hd < kMaxGroup; ++hd) {
             if (hd >= G) break;
-            const float sc = bad ? 0.f : vsc / L[hd];
+            const float sc = vsc / L[hd];
             uint2 *orow =
                 reinterpret_cast<uint2 *>(p.out + (static_cast<int64_t>(r) * p.Hq + h * G + hd) * kD) + lane;
-            *orow = make_uint2(pack_bf16x2(acc[hd].x * sc, acc[hd].y * sc),
-                               pack_bf16x2(acc[hd].z * sc, acc[hd].w * sc));
+            *orow = bad ? make_uint2(0u, 0u)
+                        : make_uint2(pack_bf16x2(acc[hd].x * sc, acc[hd].y * sc),
+                                     pack_bf16x2(acc[hd].z * sc, acc[hd].w * sc));
         }
     } else {
 #pragma unroll
@@ -569,6 +607,7 @@ __device__ void merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, in
         for (int hd = 0; hd < kMaxGroup; ++hd)
             if (hd < G && lane == hd) __stcg(p.part_ml + dst * GP + hd, make_float2(M[hd], bad ? -1.f : L[hd]));
     }
+    return true;
 }
 
 template <bool kFp8, bool kWS>
@@ -592,7 +631,8 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     // stage right after it is consumed, is ~2 % faster.
     const uint32_t full_bars = sbase + NST * Lay::kStageBytes;
     const uint32_t empty_bars = full_bars + 8 * NST;
-    const uint32_t bad_flags = empty_bars + 8 * NST;      // per stage: 1 = a page id outside the pool
+    const uint32_t merge_bar = empty_bars + 8 * NST;      // bulk copies of a shared-memory merge
+    const uint32_t bad_flags = merge_bar + 8;             // per stage: 1 = a page id outside the pool
     const int lane = threadIdx.x & 31;
     const bool producer = kWS && threadIdx.x < 32;
     const int g = lane >> 2, t = lane & 3;
@@ -604,6 +644,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             mbar_init(full_bars + 8 * s, 1);
             mbar_init(empty_bars + 8 * s, 1);
         }
+        mbar_init(merge_bar, 1);
         fence_mbar_init();
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
@@ -666,8 +707,10 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
         return;
     }
     const int64_t n_tiles = hi - lo;
-    // entries one shared-memory merge round holds (the idle stage ring)
-    const int merge_cap = (NST * Lay::kStageBytes) / (G * kD * 4 + ((G + 1) & ~1) * 8);
+    // entries one shared-memory merge round holds (the idle stage ring: outputs,
+    // statistics and weights of each; one entry per lane)
+    const int merge_cap = min(32, (NST * Lay::kStageBytes) / (G * kD * 4 + ((G + 1) & ~1) * 8 + 32));
+    uint32_t merge_phase = 0;
 #if FKV_KV_EVICT_FIRST
     const uint64_t policy = l2_policy_evict_first();
 #else
@@ -788,6 +831,58 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     wait_plan();
     zero_rows();
 
+    // Where the parts of a unit sit: its first warp and how many warps it
+    // spans.  A unit over more than kChunk warps merges in chunks of kChunk
+    // consecutive parts; c0 is the first part of this warp's chunk.
+    struct UnitGeom {
+        int wf, span;
+        __device__ int c0(int w) const { return ((w - wf) / kChunk) * kChunk; }
+        __device__ int csz(int w) const { return min(kChunk, span - c0(w)); }
+        __device__ int nch() const { return (span + kChunk - 1) / kChunk; }
+    };
+    const bool maybe_empty = T < nw;                   // warps with an empty range exist
+    auto unit_geom = [&](int r, int h) {
+        const int64_t base = p.prefix[r];
+        const int64_t nt = (p.prefix[r + 1] - base) / Hkv;
+        const int64_t s0 = base + h * nt;
+        const int64_t wf = warp_of_tile(s0, T, nw);
+        return UnitGeom{static_cast<int>(wf), static_cast<int>(warp_of_tile(s0 + nt - 1, T, nw) - wf + 1)};
+    };
+    // A merge this warp owes (kFinalDue: the single-level merge of a unit;
+    // kChunkDue: the first level of a two-level merge, then the unit's
+    // arrival and, if last, its second level), for unit (r, h).
+    int pend_stage = kNone, pend_r = 0, pend_h = 0;
+    UnitGeom pend_gm{};
+    float pend_vsc = 1.f;
+    auto merge_steps = [&](int stage, const UnitGeom &gm, int r, int h, float vsc, bool ring) {
+        auto merge = [&](int64_t sl0, int cnt, int stride, bool me, int64_t wk0, bool fin, int64_t d) {
+            if (!ring) {
+                merge_parts(p, nw, sl0, cnt, stride, me, wk0, T, fin, r, h, vsc, d);
+                return true;
+            }
+            if (merge_parts_smem(p, sbase, merge_cap, merge_bar, merge_phase, nw, sl0, cnt, stride, me, wk0, T,
+                                 fin, r, h, vsc, d))
+                return true;
+            if (lane == 0) atomicOr(p.err, FKV_DEVERR_TIMEOUT);
+            return false;
+        };
+        const int64_t u = static_cast<int64_t>(r) * Hkv + h;
+        __syncwarp();
+        if (stage == kFinalDue) {
+            merge(u + gm.wf, gm.span, 1, maybe_empty, gm.wf, true, 0);
+            return;
+        }
+        const int c0 = gm.c0(w), csz = gm.csz(w);
+        if (csz > 1 && !merge(u + gm.wf + c0, csz, 1, false, gm.wf + c0, false, u + gm.wf + c0)) return;
+        __syncwarp();
+        int last2 = 0;
+        if (lane == 0) last2 = atomic_add_acq_rel_gpu(p.counters + u, 1) == gm.nch() - 1;
+        if (__shfl_sync(kFull, last2, 0)) {
+            __syncwarp();
+            merge(u + gm.wf, gm.nch(), kChunk, false, gm.wf, true, 0);
+        }
+    };
+
     // ---------------- compute side ----------------
     uint32_t qb[8][2];
     float cfac[2] = {0.f, 0.f};
@@ -795,6 +890,8 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     float o[8][4];
     int cseq = 0, seg_start = 0;
     bool unit_bad = false;
+    float cvsc = 1.f;       // the unit's V scale
+    UnitGeom cgm{};         // where the unit's parts sit, if it is split
 
     for (int64_t i = 0; i < n_tiles; ++i) {
         const int s = static_cast<int>(i % NST);
@@ -805,6 +902,10 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             cseq = __ldg(p.seq_lens + C.r);
             seg_start = C.tt;
             unit_bad = false;
+            cvsc = kFp8 ? __ldg(p.v_scale + C.h) : 1.f;
+            // a unit that started in an earlier warp or ends in a later one is
+            // split: find its parts now, off the merge's critical path
+            if (seg_start > 0 || C.nt - C.tt > n_tiles - i) cgm = unit_geom(C.r, C.h);
             m[0] = m[1] = -INFINITY;
             l[0] = l[1] = 0.f;
 #pragma unroll
@@ -1071,7 +1172,6 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             }
             const bool whole = seg_start == 0 && C.tt == C.nt - 1;
             const int64_t u = static_cast<int64_t>(C.r) * Hkv + C.h;
-            const float vsc = kFp8 ? __ldg(p.v_scale + C.h) : 1.f;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int hd = 2 * t + j;
@@ -1086,7 +1186,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                 const int d0 = kFp8 ? 16 * g : 8 * g;          // first run of dims
                 const int d1 = kFp8 ? 16 * g + 8 : 64 + 8 * g; // second run (8 dims each)
                 if (whole) {
-                    const float f = unit_bad ? 0.f : vsc / lt[j];
+                    const float f = unit_bad ? 0.f : cvsc / lt[j];
                     __nv_bfloat16 *orow = p.out + (static_cast<int64_t>(C.r) * p.Hq + C.h * G + hd) * kD;
                     uint4 r0v, r1v;
                     r0v.x = pack_bf16x2(v[0] * f, v[1] * f);
@@ -1116,58 +1216,50 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                 // so no single warp reads a long unit's partials serially.
                 // Arrivals are acquire-release atomics by lane 0 after a warp
                 // barrier: they publish this warp's partial and, for the last
-                // arriver, make every other part visible.  At the end of the
-                // range the stage ring is idle and the merge reads through it.
-                const int64_t s0 = p.prefix[C.r] + static_cast<int64_t>(C.h) * C.nt;
-                const int64_t wf = warp_of_tile(s0, T, nw), wl = warp_of_tile(s0 + C.nt - 1, T, nw);
-                const int span = static_cast<int>(wl - wf + 1);
-                const bool maybe_empty = T < nw;
-                const bool ring_idle = i == n_tiles - 1;
-                auto merge = [&](int64_t sl0, int cnt, int stride, bool me, int64_t wk0, bool fin, int64_t d) {
-                    if (ring_idle)
-                        merge_parts_smem(p, sbase, merge_cap, nw, sl0, cnt, stride, me, wk0, T, fin, C.r, C.h, vsc, d);
-                    else
-                        merge_parts(p, nw, sl0, cnt, stride, me, wk0, T, fin, C.r, C.h, vsc, d);
-                };
+                // arriver, make every other part visible.
+                const UnitGeom &gm = cgm;
+                int stage = kNone;
                 __syncwarp();
-                if (maybe_empty || span <= kChunk) {
-                    int nparts = span;
+                if (maybe_empty || gm.span <= kChunk) {
+                    int nparts = gm.span;
                     if (maybe_empty) {
                         nparts = 0;
-                        for (int64_t x = wf; x <= wl; ++x) nparts += warp_lo(x, T, nw) != warp_lo(x + 1, T, nw);
+                        for (int64_t x = gm.wf; x < gm.wf + gm.span; ++x)
+                            nparts += warp_lo(x, T, nw) != warp_lo(x + 1, T, nw);
                     }
                     int last = 0;
                     if (lane == 0) last = atomic_add_acq_rel_gpu(p.counters + u, 1) == nparts - 1;
-                    if (__shfl_sync(kFull, last, 0)) {
-                        __syncwarp();
-                        merge(u + wf, span, 1, maybe_empty, wf, true, 0);
-                    }
+                    stage = __shfl_sync(kFull, last, 0) ? kFinalDue : kNone;
                 } else {
-                    const int c0 = (static_cast<int>(w - wf) / kChunk) * kChunk;
-                    const int csz = min(kChunk, span - c0);
-                    const int nch = (span + kChunk - 1) / kChunk;
                     // A one-part chunk (the unit's last warp, whose part ends early in
-                    // its range) is already its own result: it skips the first
-                    // level instead of merging itself mid-range.
+                    // its range) is already its own result: no first level.
+                    const int csz = gm.csz(w);
                     int last = csz == 1;
                     if (csz > 1 && lane == 0)
-                        last = atomic_add_acq_rel_gpu(p.chunk_counters + (u + wf + c0), 1) == csz - 1;
-                    if (__shfl_sync(kFull, last, 0)) {
-                        __syncwarp();
-                        if (csz > 1) merge(u + wf + c0, csz, 1, false, wf + c0, false, u + wf + c0);
-                        __syncwarp();
-                        int last2 = 0;
-                        if (lane == 0) last2 = atomic_add_acq_rel_gpu(p.counters + u, 1) == nch - 1;
-                        if (__shfl_sync(kFull, last2, 0)) {
-                            __syncwarp();
-                            merge(u + wf, nch, kChunk, false, wf, true, 0);
-                        }
+                        last = atomic_add_acq_rel_gpu(p.chunk_counters + (u + gm.wf + gm.c0(w)), 1) == csz - 1;
+                    stage = __shfl_sync(kFull, last, 0) ? kChunkDue : kNone;
+                }
+                if (stage != kNone) {
+                    if (i == n_tiles - 1) {
+                        merge_steps(stage, gm, C.r, C.h, cvsc, true);   // the stage ring is idle: merge through it
+                    } else if (FKV_DEFER_MIDRANGE && pend_stage == kNone) {
+                        // Only a range's first unit can be split and end before the
+                        // range does; its merge waits for the idle ring at the range
+                        // end instead of stalling the stream here.
+                        pend_stage = stage;
+                        pend_r = C.r;
+                        pend_h = C.h;
+                        pend_gm = gm;
+                        pend_vsc = cvsc;
+                    } else {
+                        merge_steps(stage, gm, C.r, C.h, cvsc, false);
                     }
                 }
             }
         }
         cursor_next(C, p);
     }
+    if (pend_stage != kNone) merge_steps(pend_stage, pend_gm, pend_r, pend_h, pend_vsc, true);
     grid_dep_launch();
 }
 
