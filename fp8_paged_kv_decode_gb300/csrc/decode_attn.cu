@@ -37,6 +37,7 @@
 //     empty, malformed) are zero-filled by the warps, one request each.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -76,10 +77,14 @@ constexpr uint32_t kFull = 0xffffffffu;
 #ifndef FKV_MERGE_CHUNK
 #define FKV_MERGE_CHUNK 6
 #endif
-// Merges due in the middle of a warp's range wait for its end (1) or run at
-// once through registers (0).
-#ifndef FKV_DEFER_MIDRANGE
-#define FKV_DEFER_MIDRANGE 0
+// Small batches may give each (request, KV head) unit whole warps (1) instead
+// of an even split of the batch's tiles (0); ranges then hold at least
+// FKV_ALIGNED_MIN_TILES tiles.
+#ifndef FKV_ALIGNED_SCHEDULE
+#define FKV_ALIGNED_SCHEDULE 1
+#endif
+#ifndef FKV_ALIGNED_MIN_TILES
+#define FKV_ALIGNED_MIN_TILES 2
 #endif
 #ifndef FKV_MIN_TILES_PER_WARP
 #define FKV_MIN_TILES_PER_WARP 8
@@ -87,6 +92,7 @@ constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kNone = 0, kFinalDue = 1, kChunkDue = 2;   // merge duties of a warp
 constexpr int kChunk = FKV_MERGE_CHUNK;  // parts merged per first-level merge of a long unit
 constexpr int kMinTilesPerWarp = FKV_MIN_TILES_PER_WARP;   // small batches use fewer, longer warp ranges
+constexpr int kMinAlignedTiles = FKV_ALIGNED_MIN_TILES;
 constexpr int kLocalPlanMax = 1024;
 // Attention CTA: one warp that both issues copies and computes, or (kWS) a
 // producer warp that issues copies and a consumer warp that computes.
@@ -328,6 +334,76 @@ __device__ __forceinline__ int64_t scan_requests(const RequestInfo &ri, int b, i
         fr.row0 = __shfl_sync(kFull, ri.row, src);
     }
     return __shfl_sync(kFull, inc, 31);
+}
+
+// Where the parts of a split unit sit: its first warp and how many warps it
+// spans.  A unit over more than kChunk warps merges in chunks of kChunk
+// consecutive parts; c0 is the first part of warp w's chunk.
+struct UnitGeom {
+    int wf, span;
+    __device__ int c0(int w) const { return ((w - wf) / kChunk) * kChunk; }
+    __device__ int csz(int w) const { return min(kChunk, span - c0(w)); }
+    __device__ int nch() const { return (span + kChunk - 1) / kChunk; }
+};
+
+// Schedule of a small batch (up to 64 requests, each lane holding two
+// requests' rows): every unit (request, KV head) gets whole warps, k_r =
+// ceil(n_r / tpw) of them for a request of n_r tiles per head, each holding an
+// even share of the unit's tiles.  No range then crosses a unit boundary and
+// every merge runs at a range end.  tpw is the smallest count (at least
+// kMinAlignedTiles) with which the warps fit: with U = B * Hkv units at most,
+// sum over units of ceil(n_u / tpw) < T / tpw + U <= NW once
+// tpw >= T / (NW - U).  It is used only when tpw is below kMinTilesPerWarp,
+// where the even split of the batch's tiles would leave warps idle; otherwise
+// this returns false.  Past that test every count fits in 32 bits.  Warp w
+// gets tiles [lo, hi) (empty past the last unit's warps), the request holding
+// them, and its unit's warps.
+template <int kTile>
+__device__ __forceinline__ bool place_aligned(const RequestInfo (&rc)[2], int64_t T, int B, int NW, int Hkv, int w,
+                                              int64_t &lo, int64_t &hi, FirstRequest &fr, UnitGeom &gm) {
+    const int lane = threadIdx.x & 31;
+    const int room = NW - B * Hkv;
+    if (room <= 0 || T > static_cast<int64_t>(kMinTilesPerWarp - 1) * room) return false;
+    const int tpw = max(kMinAlignedTiles, (static_cast<int>(T) + room - 1) / room);
+    lo = hi = 0;
+    int wcarry = 0, tcarry = 0;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int n = rc[c].tiles > 0 ? (rc[c].seq_len + kTile - 1) / kTile : 0;   // tiles per KV head
+        const int k = (n + tpw - 1) / tpw;                 // warps per KV head
+        const int K = k * Hkv, cnt = n * Hkv;
+        int kin = K, tin = cnt;                            // inclusive scans over the 32 requests
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, kin, o), z = __shfl_up_sync(kFull, tin, o);
+            if (lane >= o) {
+                kin += y;
+                tin += z;
+            }
+        }
+        const int wex = wcarry + kin - K;                  // this request's first warp
+        const int tex = tcarry + tin - cnt;                // and first tile
+        const unsigned hit = __ballot_sync(kFull, K > 0 && wex <= w && w < wex + K);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            const int wr = __shfl_sync(kFull, wex, src), kk = __shfl_sync(kFull, k, src);
+            const int nn = __shfl_sync(kFull, n, src), base = __shfl_sync(kFull, tex, src);
+            const int rel = w - wr, h = rel / kk, j = rel - h * kk;
+            const int s0 = base + h * nn;
+            lo = s0 + j * nn / kk;
+            hi = s0 + (j + 1) * nn / kk;
+            fr.r0 = 32 * c + src;
+            fr.base0 = base;
+            fr.nt0 = nn;
+            fr.sl0 = __shfl_sync(kFull, rc[c].seq_len, src);
+            fr.row0 = __shfl_sync(kFull, rc[c].row, src);
+            gm.wf = wr + h * kk;
+            gm.span = kk;
+        }
+        wcarry += __shfl_sync(kFull, kin, 31);
+        tcarry += __shfl_sync(kFull, tin, 31);
+    }
+    return true;
 }
 
 // The same search reading the requests 32 at a time (any batch size).
@@ -610,7 +686,13 @@ __device__ bool merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, ui
     return true;
 }
 
-template <bool kFp8, bool kWS>
+// kAligned: the instance launched for batches that the schedule with whole
+// warps per unit (place_aligned) is sure to take, by the host's bound on the
+// batch's tiles; it still checks and falls back to the even split (a page
+// table whose rows overlap can defeat the bound).  The option lives in its own
+// instance because carrying it costs the even split's streaming loop a few
+// percent.
+template <bool kFp8, bool kWS, bool kAligned>
 __global__ void __launch_bounds__(attn_threads(kWS), 1)
 paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV) {
@@ -675,6 +757,10 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     const bool local = p.B <= kLocalPlanMax;
     int64_t T;
     int nw;
+    bool aligned = false;          // small batch: every unit has whole warps
+    int64_t lo = 0, hi = 0;
+    FirstRequest afr;
+    UnitGeom agm{0, 0};            // the warp's unit, under the aligned schedule
     // Up to 64 requests: one load of every request's row (two per lane) serves
     // both the total and the search for the first request.
     const bool cached = p.B <= 64;
@@ -688,6 +774,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) T += __shfl_xor_sync(kFull, T, o);
         nw = working_warps(T, p.NW);
+        if (kAligned) aligned = place_aligned<kTile>(rc, T, p.B, p.NW, Hkv, w, lo, hi, afr, agm);
     } else if (local) {
         T = batch_tiles(p, kTile);
         nw = working_warps(T, p.NW);
@@ -696,8 +783,10 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
         T = p.prefix[p.B];
         nw = p.warp_req[p.NW];                         // warps with work (<= NW)
     }
-    const int64_t lo = w < nw ? warp_lo(w, T, nw) : 0;
-    const int64_t hi = w < nw ? warp_lo(w + 1, T, nw) : 0;
+    if (!aligned) {
+        lo = w < nw ? warp_lo(w, T, nw) : 0;
+        hi = w < nw ? warp_lo(w + 1, T, nw) : 0;
+    }
     if (lo >= hi) {
         if (!producer) {
             wait_plan();
@@ -722,11 +811,11 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     int pid_r = -1, pbase = 0, pidA = -1, pidB = -1, lseq = 0, lneed = 0;
     int64_t lrow0 = 0;
     if (local) {
-        FirstRequest fr;
-        if (cached) {
+        FirstRequest fr = afr;                         // known already under the aligned schedule
+        if (!aligned && cached) {
             const int64_t c1 = scan_requests(rc[0], 0, 0, lo, Hkv, fr);
             if (fr.r0 < 0) scan_requests(rc[1], 32, c1, lo, Hkv, fr);
-        } else {
+        } else if (!aligned) {
             fr = find_request(p, kTile, lo);
         }
         cursor_at(L, fr.r0, fr.base0, fr.nt0, lo);
@@ -831,16 +920,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     wait_plan();
     zero_rows();
 
-    // Where the parts of a unit sit: its first warp and how many warps it
-    // spans.  A unit over more than kChunk warps merges in chunks of kChunk
-    // consecutive parts; c0 is the first part of this warp's chunk.
-    struct UnitGeom {
-        int wf, span;
-        __device__ int c0(int w) const { return ((w - wf) / kChunk) * kChunk; }
-        __device__ int csz(int w) const { return min(kChunk, span - c0(w)); }
-        __device__ int nch() const { return (span + kChunk - 1) / kChunk; }
-    };
-    const bool maybe_empty = T < nw;                   // warps with an empty range exist
+    const bool maybe_empty = !aligned && T < nw;       // warps with an empty range exist
     auto unit_geom = [&](int r, int h) {
         const int64_t base = p.prefix[r];
         const int64_t nt = (p.prefix[r + 1] - base) / Hkv;
@@ -851,9 +931,6 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     // A merge this warp owes (kFinalDue: the single-level merge of a unit;
     // kChunkDue: the first level of a two-level merge, then the unit's
     // arrival and, if last, its second level), for unit (r, h).
-    int pend_stage = kNone, pend_r = 0, pend_h = 0;
-    UnitGeom pend_gm{};
-    float pend_vsc = 1.f;
     auto merge_steps = [&](int stage, const UnitGeom &gm, int r, int h, float vsc, bool ring) {
         auto merge = [&](int64_t sl0, int cnt, int stride, bool me, int64_t wk0, bool fin, int64_t d) {
             if (!ring) {
@@ -891,7 +968,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     int cseq = 0, seg_start = 0;
     bool unit_bad = false;
     float cvsc = 1.f;       // the unit's V scale
-    UnitGeom cgm{};         // where the unit's parts sit, if it is split
+    UnitGeom cgm = agm;     // where the unit's parts sit, if it is split (span 0: not yet known)
 
     for (int64_t i = 0; i < n_tiles; ++i) {
         const int s = static_cast<int>(i % NST);
@@ -905,7 +982,9 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             cvsc = kFp8 ? __ldg(p.v_scale + C.h) : 1.f;
             // a unit that started in an earlier warp or ends in a later one is
             // split: find its parts now, off the merge's critical path
-            if (seg_start > 0 || C.nt - C.tt > n_tiles - i) cgm = unit_geom(C.r, C.h);
+            // (the aligned schedule placed the warp's one unit already)
+            if ((seg_start > 0 || C.nt - C.tt > n_tiles - i) && (i > 0 || cgm.span == 0))
+                cgm = unit_geom(C.r, C.h);
             m[0] = m[1] = -INFINITY;
             l[0] = l[1] = 0.f;
 #pragma unroll
@@ -1239,27 +1318,12 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                         last = atomic_add_acq_rel_gpu(p.chunk_counters + (u + gm.wf + gm.c0(w)), 1) == csz - 1;
                     stage = __shfl_sync(kFull, last, 0) ? kChunkDue : kNone;
                 }
-                if (stage != kNone) {
-                    if (i == n_tiles - 1) {
-                        merge_steps(stage, gm, C.r, C.h, cvsc, true);   // the stage ring is idle: merge through it
-                    } else if (FKV_DEFER_MIDRANGE && pend_stage == kNone) {
-                        // Only a range's first unit can be split and end before the
-                        // range does; its merge waits for the idle ring at the range
-                        // end instead of stalling the stream here.
-                        pend_stage = stage;
-                        pend_r = C.r;
-                        pend_h = C.h;
-                        pend_gm = gm;
-                        pend_vsc = cvsc;
-                    } else {
-                        merge_steps(stage, gm, C.r, C.h, cvsc, false);
-                    }
-                }
+                // at the range end the stage ring is idle: merge through it
+                if (stage != kNone) merge_steps(stage, gm, C.r, C.h, cvsc, i == n_tiles - 1);
             }
         }
         cursor_next(C, p);
     }
-    if (pend_stage != kNone) merge_steps(pend_stage, pend_gm, pend_r, pend_h, pend_vsc, true);
     grid_dep_launch();
 }
 
@@ -1294,11 +1358,13 @@ int ctas_per_sm() {
     int &v = g_ctas_per_sm[dev][kFp8 ? 1 : 0][kWS ? 1 : 0];
     if (!v) {
         const int smem = Layout<kFp8>::kSmem;
-        if (cudaFuncSetAttribute(paged_decode_attn_kernel<kFp8, kWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem) != cudaSuccess)
+        if (cudaFuncSetAttribute(paged_decode_attn_kernel<kFp8, kWS, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+            cudaFuncSetAttribute(paged_decode_attn_kernel<kFp8, kWS, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return 0;
         int nb = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, paged_decode_attn_kernel<kFp8, kWS>,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, paged_decode_attn_kernel<kFp8, kWS, false>,
                                                           attn_threads(kWS), smem) != cudaSuccess ||
             nb <= 0)
             return 0;
@@ -1323,6 +1389,16 @@ int grid_warps(bool fp8, bool ws) {
 bool use_ws(int page_size, bool fp8) {
     const int tile = fp8 ? Layout<true>::kTile : Layout<false>::kTile;
     return page_size < (FKV_WS_PAGE_LIMIT < tile ? FKV_WS_PAGE_LIMIT : tile);
+}
+
+template <bool kFp8, bool kWS>
+cudaError_t launch_attn(bool aligned, dim3 grid, cudaStream_t st, const AttnParams &p, const CUtensorMap &tmK,
+                        const CUtensorMap &tmV) {
+    const dim3 block(attn_threads(kWS));
+    return aligned ? launch_pdl(paged_decode_attn_kernel<kFp8, kWS, true>, grid, block, Layout<kFp8>::kSmem, st, p,
+                                tmK, tmV)
+                   : launch_pdl(paged_decode_attn_kernel<kFp8, kWS, false>, grid, block, Layout<kFp8>::kSmem, st, p,
+                                tmK, tmV);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -1450,15 +1526,27 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
                                reinterpret_cast<int64_t *>(ws + wl.prefix), reinterpret_cast<int32_t *>(ws + wl.warp_req),
                                reinterpret_cast<int32_t *>(ws + wl.counters));
     if (e != cudaSuccess) return FKV_ERR_CUDA;
-    const dim3 grid(NW), block(attn_threads(two_warp));
+    // The instance with whole warps per unit serves batches the device is sure
+    // to schedule that way: a request's tiles count only when its row lists
+    // pages for all its tokens, ceil(n S / tile) <= (n S + tile - S) / tile for
+    // a row of n pages (S divides the tile or the tile divides S), so with rows
+    // that do not overlap the batch has at most
+    // Hkv (nnz S + B max(0, tile - S)) / tile tiles; place_aligned takes any
+    // batch of up to 64 requests with T <= (kMinTilesPerWarp - 1) (NW - B Hkv).
+    const int64_t room = NW - static_cast<int64_t>(batch) * num_kv_heads;
+    const int64_t tiles_bound =
+        num_kv_heads * ((nnz * page_size + static_cast<int64_t>(batch) * std::max(0, tile - page_size)) / tile);
+    const bool aligned = FKV_ALIGNED_SCHEDULE && batch <= 64 && room > 0 &&
+                         tiles_bound <= static_cast<int64_t>(kMinTilesPerWarp - 1) * room;
+    const dim3 grid(NW);
     if (fp8 && two_warp)
-        e = launch_pdl(paged_decode_attn_kernel<true, true>, grid, block, Layout<true>::kSmem, st, p, tmK, tmV);
+        e = launch_attn<true, true>(aligned, grid, st, p, tmK, tmV);
     else if (fp8)
-        e = launch_pdl(paged_decode_attn_kernel<true, false>, grid, block, Layout<true>::kSmem, st, p, tmK, tmV);
+        e = launch_attn<true, false>(aligned, grid, st, p, tmK, tmV);
     else if (two_warp)
-        e = launch_pdl(paged_decode_attn_kernel<false, true>, grid, block, Layout<false>::kSmem, st, p, tmK, tmV);
+        e = launch_attn<false, true>(aligned, grid, st, p, tmK, tmV);
     else
-        e = launch_pdl(paged_decode_attn_kernel<false, false>, grid, block, Layout<false>::kSmem, st, p, tmK, tmV);
+        e = launch_attn<false, false>(aligned, grid, st, p, tmK, tmV);
     if (e != cudaSuccess) return FKV_ERR_CUDA;
     return FKV_OK;
 }

@@ -210,11 +210,16 @@ def test_large_batches_both_schedules(orc, B, kv):
 
 
 @pytest.mark.parametrize("kv", ["fp8", "bf16"])
-@pytest.mark.parametrize("Hkv,seq", [(1, [3584]), (2, [3584]), (1, [3585]), (1, [25 * 512])])
+@pytest.mark.parametrize("Hkv,seq", [(1, [3200]), (2, [3200]), (1, [3136]), (1, [3585]), (1, [25 * 512]),
+                                     (1, [4243 * 64])])
 def test_long_unit_merge_chunks(orc, kv, Hkv, seq):
-    """One long unit split over several warps (8 tiles each): 3584 tokens are
-    56 tiles over 7 warps, so the second merge chunk holds only the unit's
-    last warp; the others give trailing chunks of other sizes."""
+    """One long unit split over many warps.  With whole warps per unit (two
+    tiles each here), 3200 tokens are 50 tiles over 25 warps: four merge
+    chunks of six parts and one that holds only the unit's last warp; 3136
+    tokens (49 tiles) give ranges of one and two tiles; 12800 tokens give 17
+    chunks, more than one shared-memory merge round holds.  4243 tiles are
+    past the whole-warp schedule on a 152-SM part: the even split, 7 to 8
+    tiles per warp."""
     case = PagedCase(orc, 1, 8 * Hkv, Hkv, 64, seq, kv=kv, seed=sum(seq) + Hkv)
     assert_close(bf16_out(case.gpu()), case.oracle(orc), "Hkv=%d seq=%s kv=%s" % (Hkv, seq, kv))
 
@@ -228,3 +233,40 @@ def test_batch_beyond_plan_smem_table(orc):
     case = PagedCase(orc, B, 2, 1, 16, seq, kv="fp8", seed=4500)
     abort = (rng.random(B) < 0.02).astype(np.uint8)
     assert_close(bf16_out(case.gpu(abort_mask=abort)), case.oracle(orc, abort_mask=abort), "B=4500")
+
+
+@pytest.mark.parametrize("kv,S", [("fp8", 64), ("fp8", 16), ("bf16", 64), ("bf16", 16)])
+@pytest.mark.parametrize("seq,abort", [
+    ([1, 64, 65], None),
+    ([30000, 100, 0, 5000, 700], [0, 1, 0, 0, 0]),
+    ([67648, 67648], None),
+    ([67712, 67712], None),
+], ids=["one_tile_units", "mixed", "whole_warp_max", "even_split_min"])
+def test_small_batch_schedules(orc, kv, S, seq, abort):
+    """Small batches give every (request, KV head) unit whole warps: units of
+    one or two tiles get one warp and need no merge, long ones are split
+    evenly over their own warps, and empty or aborted requests get none.
+    Two requests of 1057 tiles per head are the most a 152-SM part schedules
+    this way with FP8 and 64-token pages (7 tiles per warp); one tile more per
+    head, or 16-token pages (whose page count bounds the tiles more loosely),
+    takes the even split of the batch's tiles.  Page size 16 runs the
+    producer-warp CTA, 64 the single-warp one."""
+    B = len(seq)
+    case = PagedCase(orc, B, 16, 2, S, seq, kv=kv, seed=sum(seq) + S + (kv == "bf16"))
+    am = None if abort is None else np.array(abort, np.uint8)
+    got = bf16_out(case.gpu(abort_mask=am))
+    assert_close(got, case.oracle(orc, abort_mask=am), "seq=%s kv=%s S=%d" % (seq, kv, S))
+
+
+@pytest.mark.parametrize("kv", ["fp8", "bf16"])
+def test_batch_of_48_even_split(orc, kv):
+    """48 requests of 8 KV heads (384 units) is the shape of the 64-request
+    headline: the instance without the whole-warp option, each warp finding
+    its range of the even split from the requests' rows it loaded itself."""
+    rng = np.random.default_rng(48 + (kv == "bf16"))
+    seq = rng.integers(1, 3000, 48)
+    seq[[3, 17]] = 0
+    case = PagedCase(orc, 48, 64, 8, 64, seq, kv=kv, seed=480 + (kv == "bf16"))
+    abort = np.zeros(48, np.uint8)
+    abort[[5, 40]] = 1
+    assert_close(bf16_out(case.gpu(abort_mask=abort)), case.oracle(orc, abort_mask=abort), "B=48 kv=" + kv)
