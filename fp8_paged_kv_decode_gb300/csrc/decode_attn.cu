@@ -18,7 +18,7 @@
 //  2. attention (persistent, one computing warp per CTA, grid = SMs x
 //     resident CTAs): the concatenation of all units' tiles is cut into equal
 //     contiguous ranges, one per computing warp (split-KV with even load
-//     across the lognormal context mix).  For batches of up to 1024 requests
+//     across the lognormal context mix).  For batches of up to 128 requests
 //     each warp finds its own range from the inputs and starts its copies
 //     before the plan kernel has finished.  Each warp streams its tiles
 //     through a private ring of shared-memory stages filled by 128B-swizzled
@@ -93,7 +93,15 @@ constexpr int kNone = 0, kFinalDue = 1, kChunkDue = 2;   // merge duties of a wa
 constexpr int kChunk = FKV_MERGE_CHUNK;  // parts merged per first-level merge of a long unit
 constexpr int kMinTilesPerWarp = FKV_MIN_TILES_PER_WARP;   // small batches use fewer, longer warp ranges
 constexpr int kMinAlignedTiles = FKV_ALIGNED_MIN_TILES;
-constexpr int kLocalPlanMax = 1024;
+// Batches of up to this many requests are scheduled by the attention warps
+// from the inputs (at most 1024: one 32-request chunk per lane).  Past ~128
+// every warp reading all the requests' rows costs more than waiting for the
+// plan kernel's table (at 1024 requests of 256 tokens: 133 vs 122 us).
+#ifndef FKV_LOCAL_PLAN_MAX
+#define FKV_LOCAL_PLAN_MAX 128
+#endif
+constexpr int kLocalPlanMax = FKV_LOCAL_PLAN_MAX;
+static_assert(kLocalPlanMax <= 1024, "one 32-request chunk per lane");
 // Attention CTA: one warp that both issues copies and computes, or (kWS) a
 // producer warp that issues copies and a consumer warp that computes.
 __host__ __device__ constexpr int attn_threads(bool ws) { return ws ? 64 : 32; }      // batches up to this size: each warp finds its own range
@@ -292,14 +300,24 @@ __device__ __forceinline__ void cursor_at(Cursor &c, int r, int64_t base, int nt
     c.tt = static_cast<int>(rel - static_cast<int64_t>(c.h) * nt);
 }
 
-// Total tiles of the batch, computed by one warp from the inputs (the same
-// sum the plan kernel forms).
-__device__ __forceinline__ int64_t batch_tiles(const AttnParams &p, int tile) {
+// Total tiles of a batch of up to 1024 requests, computed by one warp from
+// the inputs (the same sum the plan kernel forms), reading the requests 32 at
+// a time with several chunks' loads in flight; lane c keeps in `mine` the
+// tiles of chunk c (requests 32c .. 32c + 31).
+__device__ __forceinline__ int64_t batch_tiles(const AttnParams &p, int tile, int64_t &mine) {
+    const int lane = threadIdx.x & 31;
+    const int nch = (p.B + 31) / 32;
     int64_t sum = 0;
-    for (int r = threadIdx.x & 31; r < p.B; r += 32)
-        sum += request_tiles(p.seq_lens, p.indptr, p.abort_mask, p.nnz, r, p.Hkv, p.S, tile);
+    mine = 0;
+#pragma unroll 4
+    for (int c = 0; c < nch; ++c) {
+        const int r = 32 * c + lane;
+        int64_t t = r < p.B ? request_tiles(p.seq_lens, p.indptr, p.abort_mask, p.nnz, r, p.Hkv, p.S, tile) : 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+        if (lane == c) mine = t;
+        sum += t;
+    }
     return sum;
 }
 
@@ -406,16 +424,26 @@ __device__ __forceinline__ bool place_aligned(const RequestInfo (&rc)[2], int64_
     return true;
 }
 
-// The same search reading the requests 32 at a time (any batch size).
-__device__ __forceinline__ FirstRequest find_request(const AttnParams &p, int tile, int64_t x) {
+// The same search for up to 1024 requests: the chunk holding tile x comes
+// from the per-chunk totals batch_tiles left (`mine`), then that chunk's rows
+// are read again and scanned.
+__device__ __forceinline__ FirstRequest find_request(const AttnParams &p, int tile, int64_t x, int64_t mine) {
     const int lane = threadIdx.x & 31;
+    int64_t incl = mine;                                   // inclusive scan over the chunks
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(kFull, mine > 0 && incl - mine <= x && x < incl);
     FirstRequest fr;
-    int64_t carry = 0;
-    for (int b = 0; b < p.B && fr.r0 < 0; b += 32) {
-        const int r = b + lane;
+    if (hit) {
+        const int c = __ffs(hit) - 1;
+        const int64_t carry = __shfl_sync(kFull, incl - mine, c);
+        const int r = 32 * c + lane;
         RequestInfo ri{0, 0, 0};
         if (r < p.B) ri = request_info(p.seq_lens, p.indptr, p.abort_mask, p.nnz, r, p.Hkv, p.S, tile);
-        carry += scan_requests(ri, b, carry, x, p.Hkv, fr);
+        scan_requests(ri, 32 * c, carry, x, p.Hkv, fr);
     }
     return fr;
 }
@@ -756,6 +784,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     };
     const bool local = p.B <= kLocalPlanMax;
     int64_t T;
+    int64_t chunk_tiles = 0;       // local schedule: tiles of requests 32 lane .. 32 lane + 31
     int nw;
     bool aligned = false;          // small batch: every unit has whole warps
     int64_t lo = 0, hi = 0;
@@ -776,7 +805,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
         nw = working_warps(T, p.NW);
         if (kAligned) aligned = place_aligned<kTile>(rc, T, p.B, p.NW, Hkv, w, lo, hi, afr, agm);
     } else if (local) {
-        T = batch_tiles(p, kTile);
+        T = batch_tiles(p, kTile, chunk_tiles);
         nw = working_warps(T, p.NW);
     } else {
         wait_plan();
@@ -816,7 +845,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             const int64_t c1 = scan_requests(rc[0], 0, 0, lo, Hkv, fr);
             if (fr.r0 < 0) scan_requests(rc[1], 32, c1, lo, Hkv, fr);
         } else if (!aligned) {
-            fr = find_request(p, kTile, lo);
+            fr = find_request(p, kTile, lo, chunk_tiles);
         }
         cursor_at(L, fr.r0, fr.base0, fr.nt0, lo);
         pid_r = fr.r0;                                 // the first request's page-table row is known
