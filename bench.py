@@ -337,6 +337,30 @@ class Step:
         barrier()
         return t0.elapsed_time(t1)
 
+    def timed_cold(self, reps, warmup):
+        """Median time of one captured step (append + check + attention) with
+        L2 flushed before each: a read of twice the L2 size between steps, so
+        the step reads its KV, page table and queries from HBM (a read, not a
+        write, leaves no dirty lines for the step to write back)."""
+        torch = self.torch
+        g = self.graph(True, 0, False)
+        l2 = int(getattr(torch.cuda.get_device_properties(self.device), "L2_cache_size", 0)) or (128 << 20)
+        flush = torch.ones(2 * l2 // 4, dtype=torch.int32, device=self.device)
+        sink = torch.empty((), dtype=torch.int32, device=self.device)
+        for _ in range(warmup):
+            torch.amax(flush, dim=0, out=sink)
+            g.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize(self.device)
+        for a, b in ev:
+            torch.amax(flush, dim=0, out=sink)
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize(self.device)
+        del flush
+        return float(np.median([a.elapsed_time(b) for a, b in ev]))
+
     def time_prefill(self, reps=3):
         """Bulk write of the whole cached context as a prefill would hand it
         over: kv_calibrate_scales on the bf16 prompt, then kv_append_fp8 of
@@ -640,7 +664,9 @@ def capacity_sweep(args):
     workload in BF16; how many requests each KV dtype admits under it, and the
     decode step (append + check + attention) at concurrency 1..64 for both,
     for the concurrencies each dtype can hold.  Steps are CUDA-graph captured
-    so small batches measure GPU time, not host launch cost."""
+    so small batches measure GPU time, not host launch cost; repeated steps
+    over the same pages keep a small batch's KV in L2, so each row also gives
+    the step time with L2 flushed before every step."""
     import torch
     import fp8_paged_kv_decode_gb300 as fkv
     from fp8_paged_kv_decode_gb300 import workloads as W
@@ -666,7 +692,9 @@ def capacity_sweep(args):
             st = Step(sub, kv, device)
             tot = st.timed_graph(steps, args.warmup)                 # whole step, CUDA graph
             attn = st.timed_graph(steps, args.warmup, attn_only=True)
-            row[kv] = {"step_ms": tot / steps, "tokens_per_s": c / (tot / steps / 1e3), "attn_ms": attn / steps}
+            cold = st.timed_cold(max(20, steps // 5), args.warmup)    # L2 flushed before each step
+            row[kv] = {"step_ms": tot / steps, "tokens_per_s": c / (tot / steps / 1e3), "attn_ms": attn / steps,
+                       "step_ms_cold_l2": cold}
             del st
             torch.cuda.empty_cache()
         rows.append(row)
