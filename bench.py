@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--kv", default="fp8", choices=["fp8", "bf16"], help="KV cache dtype of the main line")
     ap.add_argument("--page-size", type=int, default=None, help="override the workload's page size (tokens)")
     ap.add_argument("--ctx", default=None, help="override the workload's context lengths, e.g. fixed:16384")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's request count (the same seeded draws: the first N requests)")
     ap.add_argument("--stale-frac", type=float, default=None,
                     help="override the workload's fraction of stale (reallocated) pages, e.g. 0 for a clean batch")
     ap.add_argument("--skip-extras", action="store_true", help="only the FP8 headline and e2e")
@@ -75,8 +77,10 @@ def dist_env():
 
 
 def selected_workload(W, args):
-    """The --workload entry, with --page-size, --ctx and --stale-frac applied when given."""
+    """The --workload entry, with --batch, --page-size, --ctx and --stale-frac applied when given."""
     wl = W.WORKLOADS[args.workload]
+    if args.batch is not None and args.batch != wl.batch:
+        wl = dataclasses.replace(wl, name="%s (first %d requests)" % (wl.name, args.batch), batch=args.batch)
     if args.ctx is not None and args.ctx != wl.ctx:
         wl = dataclasses.replace(wl, name="%s (ctx %s)" % (wl.name, args.ctx), ctx=args.ctx)
     if args.page_size is not None and args.page_size != wl.page_size:
