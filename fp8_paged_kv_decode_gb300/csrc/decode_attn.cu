@@ -18,9 +18,11 @@
 //  2. attention (persistent, one computing warp per CTA, grid = SMs x
 //     resident CTAs): the concatenation of all units' tiles is cut into equal
 //     contiguous ranges, one per computing warp (split-KV with even load
-//     across the lognormal context mix).  For batches of up to 128 requests
-//     each warp finds its own range from the inputs and starts its copies
-//     before the plan kernel has finished.  Each warp streams its tiles
+//     across the lognormal context mix); a small batch instead gives each
+//     unit whole warps of its own (a separate kernel instance, chosen by the
+//     host from a bound on the batch's tiles).  For batches of up to 128
+//     requests each warp finds its own range from the inputs and starts its
+//     copies before the plan kernel has finished.  Each warp streams its tiles
 //     through a private ring of shared-memory stages filled by 128B-swizzled
 //     TMA tensor copies (one box per page: the K and V tiles of a (page, head)
 //     are contiguous in HBM); when a tile spans several small pages a second,
@@ -32,8 +34,8 @@
 //     output directly; otherwise it writes an unnormalised fp32 partial
 //     (o, m, l), and the last of the unit's warps to arrive (an atomic
 //     counter, no waiting) merges the partials with a log-sum-exp rescale
-//     (two levels for units split over many warps), through its idle stage
-//     ring at the end of its range.  Rows of requests with no tiles (aborted,
+//     (two levels for units split over many warps), fetching them with 1-D
+//     bulk copies into its idle stage ring at the end of its range.  Rows of requests with no tiles (aborted,
 //     empty, malformed) are zero-filled by the warps, one request each.
 #include <cudaTypedefs.h>
 
