@@ -59,3 +59,27 @@ def test_fuzz_against_oracle(orc, case_id):
     case.indptr = indptr
     got = bf16_out(case.gpu(abort_mask=use_mask, indices=ind))
     assert_close(got, ref, "fuzz case %d: B=%d Hq=%d Hkv=%d S=%d kv=%s seq=%s" % (case_id, B, Hq, Hkv, S, kv, seq))
+
+
+N_MEDIUM = 12
+
+
+@pytest.mark.parametrize("case_id", range(N_MEDIUM))
+def test_fuzz_medium_batches(orc, case_id):
+    """Seeded batches of 40 to 200 requests with short, ragged contexts: the
+    even split scheduled from each warp's own reading of the requests' rows
+    (up to 64 requests in one load, up to 128 in 32-request chunks) and from
+    the plan kernel's table (beyond 128), with empty and aborted requests."""
+    rng = np.random.default_rng(9500 + case_id)
+    B = int(rng.integers(40, 201))
+    G = int(rng.choice([1, 2, 4, 8]))
+    Hkv = int(rng.choice([2, 4, 8]))
+    S = int(rng.choice([16, 32, 64, 128]))
+    special = [0, 1, S - 1, S, S + 1, 63, 64, 65]
+    seq = [int(rng.choice(special)) if rng.random() < 0.3 else int(rng.integers(1, 700)) for _ in range(B)]
+    kv = "bf16" if rng.random() < 0.3 else "fp8"
+    case = PagedCase(orc, B, G * Hkv, Hkv, S, seq, kv=kv, seed=9600 + case_id)
+    abort = (rng.random(B) < 0.05).astype(np.uint8)
+    got = bf16_out(case.gpu(abort_mask=abort))
+    assert_close(got, case.oracle(orc, abort_mask=abort),
+                 "medium fuzz %d: B=%d Hq=%d Hkv=%d S=%d kv=%s" % (case_id, B, G * Hkv, Hkv, S, kv))
