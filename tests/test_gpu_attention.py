@@ -273,3 +273,16 @@ def test_batch_of_48_even_split(orc, kv):
     abort = np.zeros(48, np.uint8)
     abort[[5, 40]] = 1
     assert_close(bf16_out(case.gpu(abort_mask=abort)), case.oracle(orc, abort_mask=abort), "B=48 kv=" + kv)
+
+
+@pytest.mark.parametrize("kv", ["fp8", "bf16"])
+@pytest.mark.parametrize("S", [16, 64])
+def test_batch_with_no_live_request(orc, kv, S):
+    """Every request empty or aborted: the host's tile bound sends the batch
+    to the whole-warp instance, no warp gets work, and every output row (the
+    buffer starts as NaN) must still come out zero."""
+    case = PagedCase(orc, 4, 16, 2, S, [100, 0, 300, 0], kv=kv, seed=77 + S)
+    am = np.array([1, 0, 1, 0], np.uint8)
+    got = bf16_out(case.gpu(abort_mask=am))
+    assert np.array_equal(got, np.zeros_like(got))
+    assert np.array_equal(case.oracle(orc, abort_mask=am), np.zeros_like(got))
