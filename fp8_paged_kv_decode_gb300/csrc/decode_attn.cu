@@ -70,7 +70,8 @@
 namespace fkv {
 
 constexpr int kD = 128;
-constexpr int kMaxGroup = 8;             // query heads sharing a KV head (MMA N)
+constexpr int kMaxGroup = 8;             // query heads of one unit (MMA N)
+constexpr int kMaxSplit = 8;             // virtual KV heads per KV head (group sizes up to 64)
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanSmemPrefix = 4096;    // requests whose prefix the plan searches in smem
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // a copy that has not landed in 2 s has failed
@@ -155,7 +156,12 @@ struct AttnParams {
     int32_t *chunk_counters;   // [slots] arrivals per first-level chunk, indexed by its first slot
     __nv_bfloat16 *out;
     uint32_t *err;
+    // Hkv, G: units per request and query heads per unit.  With more than
+    // kMaxGroup query heads per KV head each KV head is served as 2^hshift
+    // virtual heads of G query heads (consecutive query rows) that read the
+    // same pages: unit head h reads KV head h >> hshift.
     int B, Hq, Hkv, G, GP, P, S, NW;   // GP = G rounded up to even: 16-byte statistics rows
+    int hshift;
     float sm_scale_log2;
 };
 
@@ -914,8 +920,10 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                 const uint32_t dv = dk + Lay::kTileBytes;
 #pragma unroll
                 for (int half = 0; half < Lay::kHalves; ++half) {
-                    tma_load_4d(dk + half * Lay::kHalfBytes, &tmK, bar, half * 64, rowoff, L.h, ids[k], policy);
-                    tma_load_4d(dv + half * Lay::kHalfBytes, &tmV, bar, half * 64, rowoff, L.h, ids[k], policy);
+                    tma_load_4d(dk + half * Lay::kHalfBytes, &tmK, bar, half * 64, rowoff, L.h >> p.hshift, ids[k],
+                                policy);
+                    tma_load_4d(dv + half * Lay::kHalfBytes, &tmV, bar, half * 64, rowoff, L.h >> p.hshift, ids[k],
+                                policy);
                 }
             }
         }
@@ -1010,7 +1018,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             cseq = __ldg(p.seq_lens + C.r);
             seg_start = C.tt;
             unit_bad = false;
-            cvsc = kFp8 ? __ldg(p.v_scale + C.h) : 1.f;
+            cvsc = kFp8 ? __ldg(p.v_scale + (C.h >> p.hshift)) : 1.f;
             // a unit that started in an earlier warp or ends in a later one is
             // split: find its parts now, off the merge's critical path
             // (the aligned schedule placed the warp's one unit already)
@@ -1058,7 +1066,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                     qb[ks][0] = pack_f16x2(__uint_as_float(w0 << 16) * sc, __uint_as_float(w0 & 0xFFFF0000u) * sc);
                     qb[ks][1] = pack_f16x2(__uint_as_float(w1 << 16) * sc, __uint_as_float(w1 & 0xFFFF0000u) * sc);
                 }
-                const float ksc = __ldg(p.k_scale + C.h) * p.sm_scale_log2;
+                const float ksc = __ldg(p.k_scale + (C.h >> p.hshift)) * p.sm_scale_log2;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int ej = __shfl_sync(kFull, e, (2 * t + j) * 4);
@@ -1438,6 +1446,15 @@ struct WsLayout {
     size_t prefix, warp_req, counters, part_ml, part_o, total;
 };
 
+// Virtual KV heads per KV head for a group of G query heads: the smallest
+// power of two R with G % R == 0 and G / R <= kMaxGroup (1 up to 8 query
+// heads); 0 if there is none within kMaxSplit.
+int group_split(int G) {
+    for (int r = 1; r <= kMaxSplit; r <<= 1)
+        if (G % r == 0 && G / r <= kMaxGroup) return r;
+    return 0;
+}
+
 WsLayout ws_layout(int B, int Hkv, int G, int NW) {
     WsLayout L;
     const size_t units = static_cast<size_t>(B) * Hkv;
@@ -1477,14 +1494,14 @@ extern "C" size_t paged_decode_attn_workspace_size(int32_t batch, int32_t num_q_
                                                    int32_t head_dim, int32_t kv_dtype) {
     if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;
     if (head_dim != kD || (kv_dtype != FKV_KV_FP8_E4M3 && kv_dtype != FKV_KV_BF16)) return 0;
-    const int G = num_q_heads / num_kv_heads;
-    if (G > kMaxGroup) return 0;
+    const int R = group_split(num_q_heads / num_kv_heads);
+    if (R == 0) return 0;
     // sized for either CTA shape (the page size is not known here)
     const bool fp8 = kv_dtype == FKV_KV_FP8_E4M3;
     const int n1 = grid_warps(fp8, false), n2 = grid_warps(fp8, true);
     const int NW = n1 > n2 ? n1 : n2;
     if (n1 <= 0 || n2 <= 0) return 0;
-    return ws_layout(batch, num_kv_heads, G, NW).total;
+    return ws_layout(batch, num_kv_heads * R, num_q_heads / num_kv_heads / R, NW).total;
 }
 
 extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t num_q_heads, const void *k_cache,
@@ -1499,8 +1516,10 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
     if (kv_dtype != FKV_KV_FP8_E4M3 && kv_dtype != FKV_KV_BF16) return FKV_ERR_INVALID_ARG;
     if (head_dim != kD) return FKV_ERR_UNSUPPORTED;
     if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return FKV_ERR_UNSUPPORTED;
-    const int G = num_q_heads / num_kv_heads;
-    if (G > kMaxGroup) return FKV_ERR_UNSUPPORTED;
+    // units are (request, virtual KV head) pairs of G query heads each
+    const int R = group_split(num_q_heads / num_kv_heads);
+    if (R == 0) return FKV_ERR_UNSUPPORTED;
+    const int Hv = num_kv_heads * R, G = num_q_heads / Hv;
     if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return FKV_ERR_INVALID_ARG;
     if (batch == 0) return FKV_OK;
     const bool fp8 = kv_dtype == FKV_KV_FP8_E4M3;
@@ -1514,7 +1533,7 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
     const int NW = grid_warps(fp8, two_warp);
     uint32_t *err = device_error_word();
     if (NW <= 0 || !err) return FKV_ERR_CUDA;
-    const WsLayout wl = ws_layout(batch, num_kv_heads, G, NW);
+    const WsLayout wl = ws_layout(batch, Hv, G, NW);
     if (workspace_bytes < wl.total) return FKV_ERR_INVALID_ARG;
     const int tile = fp8 ? Layout<true>::kTile : Layout<false>::kTile;
 
@@ -1536,14 +1555,15 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
     p.prefix = reinterpret_cast<const int64_t *>(ws + wl.prefix);
     p.warp_req = reinterpret_cast<const int32_t *>(ws + wl.warp_req);
     p.counters = reinterpret_cast<int32_t *>(ws + wl.counters);
-    p.chunk_counters = p.counters + static_cast<int64_t>(batch) * num_kv_heads;
+    p.chunk_counters = p.counters + static_cast<int64_t>(batch) * Hv;
     p.part_ml = reinterpret_cast<float2 *>(ws + wl.part_ml);
     p.part_o = reinterpret_cast<float *>(ws + wl.part_o);
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.err = err;
     p.B = batch;
     p.Hq = num_q_heads;
-    p.Hkv = num_kv_heads;
+    p.Hkv = Hv;
+    p.hshift = __builtin_ctz(static_cast<unsigned>(R));
     p.G = G;
     p.GP = (G + 1) & ~1;
     p.P = num_pages;
@@ -1553,7 +1573,7 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_pdl(attn_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, seq_lens, page_indptr,
-                               abort_mask, nnz, batch, num_kv_heads, page_size, tile, NW,
+                               abort_mask, nnz, batch, Hv, page_size, tile, NW,
                                reinterpret_cast<int64_t *>(ws + wl.prefix), reinterpret_cast<int32_t *>(ws + wl.warp_req),
                                reinterpret_cast<int32_t *>(ws + wl.counters));
     if (e != cudaSuccess) return FKV_ERR_CUDA;
@@ -1562,11 +1582,12 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
     // pages for all its tokens, ceil(n S / tile) <= (n S + tile - S) / tile for
     // a row of n pages (S divides the tile or the tile divides S), so with rows
     // that do not overlap the batch has at most
-    // Hkv (nnz S + B max(0, tile - S)) / tile tiles; place_aligned takes any
-    // batch of up to 64 requests with T <= (kMinTilesPerWarp - 1) (NW - B Hkv).
-    const int64_t room = NW - static_cast<int64_t>(batch) * num_kv_heads;
+    // Hv (nnz S + B max(0, tile - S)) / tile tiles (Hv units per request);
+    // place_aligned takes any batch of up to 64 requests with
+    // T <= (kMinTilesPerWarp - 1) (NW - B Hv).
+    const int64_t room = NW - static_cast<int64_t>(batch) * Hv;
     const int64_t tiles_bound =
-        num_kv_heads * ((nnz * page_size + static_cast<int64_t>(batch) * std::max(0, tile - page_size)) / tile);
+        Hv * ((nnz * page_size + static_cast<int64_t>(batch) * std::max(0, tile - page_size)) / tile);
     const bool aligned = FKV_ALIGNED_SCHEDULE && batch <= 64 && room > 0 &&
                          tiles_bound <= static_cast<int64_t>(kMinTilesPerWarp - 1) * room;
     const dim3 grid(NW);

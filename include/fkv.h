@@ -58,7 +58,7 @@ extern "C" {
 typedef enum {
     FKV_OK = 0,
     FKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment, small workspace */
-    FKV_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim != 128, group > 8, ...) */
+    FKV_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim != 128, a group size that does not split into groups of <= 8, ...) */
     FKV_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
     FKV_ERR_SCRATCH_LIMIT = 4  /* paged_decode_attn_noalloc: the shape needs more scratch than
                                   FKV_NOALLOC_SCRATCH_BYTES */
@@ -220,7 +220,11 @@ FKV_API size_t paged_decode_attn_workspace_size(int32_t batch, int32_t num_q_hea
  * [0, num_pages), gets an all-zero output row; its pages are not read (an
  * out-of-range id is never dereferenced) and no other row is affected.
  * Supported: head_dim 128, page_size in {16, 32, 64, 128}, group size
- * num_q_heads / num_kv_heads in 1..8.
+ * G = num_q_heads / num_kv_heads in 1..8, or above 8 when G splits into R
+ * equal groups of at most 8 with R a power of two up to 8 (10, 12, 16, 24,
+ * 32, 64, ...): each group is then served as a virtual KV head that reads
+ * the KV head's pages again, so such a call reads R times the K/V bytes.
+ * Other G return FKV_ERR_UNSUPPORTED.
  */
 FKV_API fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t num_q_heads,
                              const void *k_cache, const void *v_cache, int32_t kv_dtype,

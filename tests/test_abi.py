@@ -60,7 +60,9 @@ def test_host_validation_without_gpu(lib_path):
                                  0.1, None, None, 0, None) == 2
     assert lib.paged_decode_attn(None, 2, 8, None, None, 0, None, None, 4, 3, 16, 128, None, None, 0, None, None,
                                  0.1, None, None, 0, None) == 1
+    assert lib.paged_decode_attn(None, 2, 18, None, None, 0, None, None, 4, 2, 16, 128, None, None, 0, None, None,
+                                 0.1, None, None, 0, None) == 2     # group 9: no split into groups of <= 8
     assert lib.paged_decode_attn(None, 2, 32, None, None, 0, None, None, 4, 2, 16, 128, None, None, 0, None, None,
-                                 0.1, None, None, 0, None) == 2     # group 16 > 8
+                                 0.1, None, None, 0, None) == 1     # group 16 (two groups of 8): null pointers
     assert lib.paged_decode_attn(None, 2, 8, None, None, 0, None, None, 4, 2, 16, 128, None, None, 0, None, None,
                                  -1.0, None, None, 0, None) == 1    # sm_scale must be positive

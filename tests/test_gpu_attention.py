@@ -286,3 +286,28 @@ def test_batch_with_no_live_request(orc, kv, S):
     got = bf16_out(case.gpu(abort_mask=am))
     assert np.array_equal(got, np.zeros_like(got))
     assert np.array_equal(case.oracle(orc, abort_mask=am), np.zeros_like(got))
+
+
+@pytest.mark.parametrize("kv", ["fp8", "bf16"])
+@pytest.mark.parametrize("Hq,Hkv,S,seq", [
+    (32, 2, 64, [700, 3000, 65]),        # G = 16: two groups of 8 per KV head
+    (24, 2, 16, [1, 500, 129, 2048]),    # G = 12: two groups of 6
+    (32, 1, 32, [5000, 17]),             # G = 32: four groups of 8
+    (64, 1, 64, [1500]),                 # G = 64: eight groups of 8
+    (40, 4, 64, [300] * 40),             # G = 10, 40 requests: the even split
+], ids=["g16", "g12", "g32", "g64", "g10_b40"])
+def test_large_group_sizes(orc, kv, Hq, Hkv, S, seq):
+    """Group sizes above 8 that split into a power-of-two number of groups of
+    at most 8: each group is a virtual KV head reading the KV head's pages
+    again, and every query row still matches the oracle."""
+    case = PagedCase(orc, len(seq), Hq, Hkv, S, seq, kv=kv, seed=7 * Hq + Hkv + (kv == "bf16"))
+    assert_close(bf16_out(case.gpu()), case.oracle(orc), "Hq=%d Hkv=%d S=%d kv=%s" % (Hq, Hkv, S, kv))
+
+
+def test_unsplittable_group_size_is_unsupported(orc):
+    """G = 9 has no power-of-two split into groups of at most 8: the call is
+    refused before anything is launched."""
+    import fp8_paged_kv_decode_gb300 as fkv
+    case = PagedCase(orc, 2, 9, 1, 64, [100, 200], seed=9)
+    with pytest.raises(fkv.FkvError, match="unsupported"):
+        case.gpu()
