@@ -373,12 +373,14 @@ def _numpy_reference(c, sm_scale):
 def pin_attn_vs_numpy_dense(orc):
     rng = np.random.default_rng(21)
     sm = 1.0 / np.sqrt(128.0)
-    for fp8 in (True, False):
-        c = _rand_case(rng, 3, 8, 2, 16, [1, 37, 70], fp8=fp8)
-        got = orc.paged_decode_attn(c["q"], c["k"], c["v"], c["indptr"], c["indices"], c["seq"], sm,
-                                    k_scale=c["ks"], v_scale=c["vs"])
-        want = _numpy_reference(c, sm)
-        assert np.allclose(got, want, rtol=1e-11, atol=1e-13), "fp8=%s" % fp8
+    # (Hq, Hkv): group 4, group 16 (query head i reads KV head i // 16), group 1
+    for Hq, Hkv in ((8, 2), (32, 2), (3, 3)):
+        for fp8 in (True, False):
+            c = _rand_case(rng, 3, Hq, Hkv, 16, [1, 37, 70], fp8=fp8)
+            got = orc.paged_decode_attn(c["q"], c["k"], c["v"], c["indptr"], c["indices"], c["seq"], sm,
+                                        k_scale=c["ks"], v_scale=c["vs"])
+            want = _numpy_reference(c, sm)
+            assert np.allclose(got, want, rtol=1e-11, atol=1e-13), "Hq=%d Hkv=%d fp8=%s" % (Hq, Hkv, fp8)
 
 
 def pin_attn_single_token_returns_v(orc):
