@@ -45,14 +45,21 @@ constexpr int kTokensPerBlock = kBlock / kThreadsPerToken;   // 16
 // at least 2^-111).  Below 2^-64, |a/b| < 2^-34 and both this and the exact
 // quotient give a zero code; such inputs only need a finite, correctly signed
 // result, which the sequence gives.  Anything else (a huge or non-finite a,
-// a scale out of range) takes __fdiv_rn.  The sequence runs on |a| and the
-// sign is put back afterwards, so -0 and tiny negatives keep their sign.
-__device__ __forceinline__ float div_by_recip(float a, float b, float y) {
+// a scale out of range) takes __fdiv_rn.  The sequence runs on |a|; the
+// caller puts the sign back on the e4m3 code (sign-magnitude, and rounding
+// to nearest even is symmetric), so -0 and tiny negatives keep their sign.
+__device__ __forceinline__ float div_abs_by_recip(float a, float b, float y) {
     const float m = fabsf(a);
     const float q0 = __fmul_rn(m, y);
     const float r = __fmaf_rn(-q0, b, m);
-    const float q = __fmaf_rn(r, y, q0);
-    return __uint_as_float(__float_as_uint(q) | (__float_as_uint(a) & 0x80000000u));
+    return __fmaf_rn(r, y, q0);
+}
+
+// Lane-wise maximum of two pairs of unsigned 16-bit values.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 __device__ __forceinline__ bool recip_scale_ok(float b) {
@@ -103,21 +110,23 @@ kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ 
     const uint4 r0 = __ldcs(src), r1 = __ldcs(src + 1);
     const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
     const float b = __ldg((is_v ? v_scale : k_scale) + h);
-    uint32_t big = 0;                                          // largest |x| bit pattern
+    uint32_t big = 0;                                          // largest |x| bit patterns, per half
 #pragma unroll
-    for (int j = 0; j < 8; ++j) big = max(big, max(w[j] & 0x7FFF0000u, (w[j] << 16) & 0x7FFF0000u));
+    for (int j = 0; j < 8; ++j) big = max_u16x2(big, w[j] & 0x7FFF7FFFu);
     // word j holds elements 2j (low half) and 2j+1; packed word p holds codes 4p .. 4p+3
     uint32_t packed[4];
-    if (recip_scale_ok(b) && big <= 0x5F800000u) {             // |x| <= 2^64 (finite)
+    if (recip_scale_ok(b) && (big >> 16) <= 0x5F80u && (big & 0xFFFFu) <= 0x5F80u) {   // |x| <= 2^64
         const float y = __frcp_rn(b);
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             const uint32_t u0 = w[2 * p], u1 = w[2 * p + 1];
-            const uint16_t lo = f32x2_to_e4m3x2(div_by_recip(__uint_as_float(u0 & 0xFFFF0000u), b, y),
-                                                div_by_recip(__uint_as_float(u0 << 16), b, y));
-            const uint16_t hi = f32x2_to_e4m3x2(div_by_recip(__uint_as_float(u1 & 0xFFFF0000u), b, y),
-                                                div_by_recip(__uint_as_float(u1 << 16), b, y));
-            packed[p] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+            const uint16_t lo = f32x2_to_e4m3x2(div_abs_by_recip(__uint_as_float(u0 & 0xFFFF0000u), b, y),
+                                                div_abs_by_recip(__uint_as_float(u0 << 16), b, y));
+            const uint16_t hi = f32x2_to_e4m3x2(div_abs_by_recip(__uint_as_float(u1 & 0xFFFF0000u), b, y),
+                                                div_abs_by_recip(__uint_as_float(u1 << 16), b, y));
+            // the four elements' sign bits: bit 7 of each bf16's high byte
+            const uint32_t sgn = prmt(u0, u1, 0x7531u) & 0x80808080u;
+            packed[p] = (static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16)) | sgn;
         }
     } else {
 #pragma unroll
