@@ -377,18 +377,23 @@ struct UnitGeom {
 // ceil(n_r / tpw) of them for a request of n_r tiles per head, each holding an
 // even share of the unit's tiles.  No range then crosses a unit boundary and
 // every merge runs at a range end.  tpw is the smallest count (at least
-// kMinAlignedTiles) with which the warps fit: with U = B * Hkv units at most,
-// sum over units of ceil(n_u / tpw) < T / tpw + U <= NW once
-// tpw >= T / (NW - U).  It is used only when tpw is below kMinTilesPerWarp,
-// where the even split of the batch's tiles would leave warps idle; otherwise
-// this returns false.  Past that test every count fits in 32 bits.  Warp w
+// kMinAlignedTiles) with which the warps fit: with U live units (requests
+// with tiles, times Hkv), sum over units of ceil(n_u / tpw) < T / tpw + U <=
+// NW once tpw >= T / (NW - U).  It is used only when tpw is below
+// kMinTilesPerWarp, where the even split of the batch's tiles would leave
+// warps idle; otherwise this returns false.  Both the test and tpw depend on
+// the live requests only, so an aborted request changes nothing for the
+// others.  Past the test every count fits in 32 bits.  Warp w
 // gets tiles [lo, hi) (empty past the last unit's warps), the request holding
 // them, and its unit's warps.
 template <int kTile>
-__device__ __forceinline__ bool place_aligned(const RequestInfo (&rc)[2], int64_t T, int B, int NW, int Hkv, int w,
+__device__ __forceinline__ bool place_aligned(const RequestInfo (&rc)[2], int64_t T, int NW, int Hkv, int w,
                                               int64_t &lo, int64_t &hi, FirstRequest &fr, UnitGeom &gm) {
     const int lane = threadIdx.x & 31;
-    const int room = NW - B * Hkv;
+    int live = (rc[0].tiles > 0) + (rc[1].tiles > 0);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) live += __shfl_xor_sync(kFull, live, o);
+    const int room = NW - live * Hkv;
     if (room <= 0 || T > static_cast<int64_t>(kMinTilesPerWarp - 1) * room) return false;
     const int tpw = max(kMinAlignedTiles, (static_cast<int>(T) + room - 1) / room);
     lo = hi = 0;
@@ -811,7 +816,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) T += __shfl_xor_sync(kFull, T, o);
         nw = working_warps(T, p.NW);
-        if (kAligned) aligned = place_aligned<kTile>(rc, T, p.B, p.NW, Hkv, w, lo, hi, afr, agm);
+        if (kAligned) aligned = place_aligned<kTile>(rc, T, p.NW, Hkv, w, lo, hi, afr, agm);
     } else if (local) {
         T = batch_tiles(p, kTile, chunk_tiles);
         nw = working_warps(T, p.NW);
@@ -1584,7 +1589,7 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
     // that do not overlap the batch has at most
     // Hv (nnz S + B max(0, tile - S)) / tile tiles (Hv units per request);
     // place_aligned takes any batch of up to 64 requests with
-    // T <= (kMinTilesPerWarp - 1) (NW - B Hv).
+    // T <= (kMinTilesPerWarp - 1) (NW - U Hv) for its U <= B live requests.
     const int64_t room = NW - static_cast<int64_t>(batch) * Hv;
     const int64_t tiles_bound =
         Hv * ((nnz * page_size + static_cast<int64_t>(batch) * std::max(0, tile - page_size)) / tile);

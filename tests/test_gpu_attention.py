@@ -311,3 +311,31 @@ def test_unsplittable_group_size_is_unsupported(orc):
     case = PagedCase(orc, 2, 9, 1, 64, [100, 200], seed=9)
     with pytest.raises(fkv.FkvError, match="unsupported"):
         case.gpu()
+
+
+def test_abort_equals_absent_under_whole_warp_schedule(orc):
+    """Both runs take the whole-warp schedule, and its tiles per warp come from
+    the live units only: 147 live tiles per KV head (requests of 100 and 47
+    tiles) over 8 KV heads give 1176 tiles, which would be 3 tiles per warp
+    if the aborted request's 8 units were counted (608 - 24 warps to spare on
+    a 152-SM part) and are 2 either way when only live units count.  The
+    live rows must be byte-identical to the batch without the request."""
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    case = PagedCase(orc, 3, 64, 8, 64, [6400, 64, 3008], seed=12)
+    am = np.array([0, 1, 0], np.uint8)
+    full = case.gpu(abort_mask=am).cpu()
+    keep = [0, 2]
+    indptr = [0]
+    ind = []
+    for r in keep:
+        ind.extend(case.indices[case.indptr[r]:case.indptr[r + 1]].tolist())
+        indptr.append(len(ind))
+    q = dev(case.q[keep], dtype=torch.bfloat16)
+    out = torch.empty(len(keep), 64, 128, dtype=torch.bfloat16, device="cuda")
+    ws = fkv.alloc_workspace(len(keep), 64, 8)
+    fkv.paged_decode_attn(q, dev(case.kc), dev(case.vc), dev(np.array(indptr, np.int32)), dev(np.array(ind, np.int32)),
+                          dev(case.seq[keep]), case.sm, out, ws, k_scale=dev(case.k_scale), v_scale=dev(case.v_scale))
+    torch.cuda.synchronize()
+    assert np.array_equal(full[keep].view(torch.int16).numpy(), out.cpu().view(torch.int16).numpy())
+    assert_close(bf16_out(full), case.oracle(orc, abort_mask=am), "aborted middle request")
