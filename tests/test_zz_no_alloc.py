@@ -37,10 +37,18 @@ def _noalloc(case):
 def test_noalloc_matches_regular_entry_point_twice(orc, kv):
     first = PagedCase(orc, 6, 64, 8, 64, [40000, 17, 3000, 1, 9000, 640], kv=kv, seed=501)
     second = PagedCase(orc, 4, 32, 8, 16, [4097, 33, 2, 1500], kv=kv, seed=502)
-    for case in (first, second):                     # two calls in a row share the scratch
+    third = PagedCase(orc, 3, 32, 2, 64, [5000, 40, 2100], kv=kv, seed=503)   # 16 query heads per KV head
+    for case in (first, second, third):              # calls in a row share the scratch
         want = bf16_out(case.gpu())                  # regular entry point, caller-provided workspace
         got = bf16_out(_noalloc(case))
         assert_close(got, want, "noalloc vs regular (%s, B=%d)" % (kv, case.B))
+
+
+def test_workspace_of_a_split_group():
+    """A group of 16 query heads per KV head is served as two groups of 8: the
+    workspace is that of twice the KV heads with 8 query heads each."""
+    import fp8_paged_kv_decode_gb300 as fkv
+    assert fkv.paged_decode_attn_workspace_size(3, 32, 2) == fkv.paged_decode_attn_workspace_size(3, 32, 4) > 0
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
