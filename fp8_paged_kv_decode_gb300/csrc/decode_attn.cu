@@ -39,7 +39,6 @@
 //     empty, malformed) are zero-filled by the warps, one request each.
 #include <cudaTypedefs.h>
 
-#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -727,12 +726,10 @@ __device__ bool merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, ui
     return true;
 }
 
-// kAligned: the instance launched for batches that the schedule with whole
-// warps per unit (place_aligned) is sure to take, by the host's bound on the
-// batch's tiles; it still checks and falls back to the even split (a page
-// table whose rows overlap can defeat the bound).  The option lives in its own
-// instance because carrying it costs the even split's streaming loop a few
-// percent.
+// kAligned: the instance for batches of up to 64 requests, which gives units
+// whole warps (place_aligned) when the live requests' tiles pass its test and
+// uses the even split otherwise.  Larger batches use the instance without
+// the option (their warps do not hold the requests' rows).
 template <bool kFp8, bool kWS, bool kAligned>
 __global__ void __launch_bounds__(attn_threads(kWS), 1)
 paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmK,
@@ -1582,19 +1579,11 @@ extern "C" fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t nu
                                reinterpret_cast<int64_t *>(ws + wl.prefix), reinterpret_cast<int32_t *>(ws + wl.warp_req),
                                reinterpret_cast<int32_t *>(ws + wl.counters));
     if (e != cudaSuccess) return FKV_ERR_CUDA;
-    // The instance with whole warps per unit serves batches the device is sure
-    // to schedule that way: a request's tiles count only when its row lists
-    // pages for all its tokens, ceil(n S / tile) <= (n S + tile - S) / tile for
-    // a row of n pages (S divides the tile or the tile divides S), so with rows
-    // that do not overlap the batch has at most
-    // Hv (nnz S + B max(0, tile - S)) / tile tiles (Hv units per request);
-    // place_aligned takes any batch of up to 64 requests with
-    // T <= (kMinTilesPerWarp - 1) (NW - U Hv) for its U <= B live requests.
-    const int64_t room = NW - static_cast<int64_t>(batch) * Hv;
-    const int64_t tiles_bound =
-        Hv * ((nnz * page_size + static_cast<int64_t>(batch) * std::max(0, tile - page_size)) / tile);
-    const bool aligned = FKV_ALIGNED_SCHEDULE && batch <= 64 && room > 0 &&
-                         tiles_bound <= static_cast<int64_t>(kMinTilesPerWarp - 1) * room;
+    // Every batch of up to 64 requests (whose rows the warps hold two per
+    // lane) goes to the instance that may give units whole warps; the warps
+    // decide from the live requests alone, so the schedule never depends on
+    // aborted or empty requests.
+    const bool aligned = FKV_ALIGNED_SCHEDULE && batch <= 64;
     const dim3 grid(NW);
     if (fp8 && two_warp)
         e = launch_attn<true, true>(aligned, grid, st, p, tmK, tmV);

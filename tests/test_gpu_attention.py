@@ -250,10 +250,9 @@ def test_small_batch_schedules(orc, kv, S, seq, abort):
     one or two tiles get one warp and need no merge, long ones are split
     evenly over their own warps, and empty or aborted requests get none.
     Two requests of 1057 tiles per head are the most a 152-SM part schedules
-    this way with FP8 and 64-token pages (7 tiles per warp); one tile more per
-    head, or 16-token pages (whose page count bounds the tiles more loosely),
-    takes the even split of the batch's tiles.  Page size 16 runs the
-    producer-warp CTA, 64 the single-warp one."""
+    this way with FP8 (7 tiles per warp); one tile more per head takes the
+    even split of the batch's tiles.  Page size 16 runs the producer-warp
+    CTA, 64 the single-warp one."""
     B = len(seq)
     case = PagedCase(orc, B, 16, 2, S, seq, kv=kv, seed=sum(seq) + S + (kv == "bf16"))
     am = None if abort is None else np.array(abort, np.uint8)
@@ -278,9 +277,9 @@ def test_batch_of_48_even_split(orc, kv):
 @pytest.mark.parametrize("kv", ["fp8", "bf16"])
 @pytest.mark.parametrize("S", [16, 64])
 def test_batch_with_no_live_request(orc, kv, S):
-    """Every request empty or aborted: the host's tile bound sends the batch
-    to the whole-warp instance, no warp gets work, and every output row (the
-    buffer starts as NaN) must still come out zero."""
+    """Every request empty or aborted: the batch runs the whole-warp
+    instance, no warp gets work, and every output row (the buffer starts as
+    NaN) must still come out zero."""
     case = PagedCase(orc, 4, 16, 2, S, [100, 0, 300, 0], kv=kv, seed=77 + S)
     am = np.array([1, 0, 1, 0], np.uint8)
     got = bf16_out(case.gpu(abort_mask=am))
