@@ -14,6 +14,9 @@ Parity status of each function (what pins it independently of itself is in
   saturation, NaN/Inf/-0, and torch's float8_e4m3fn for in-range values.
 * ``kv_append_fp8`` -- pinned: numpy's IEEE float32 division, slot placement
   against a hand-computed position, untouched bytes.
+* ``kv_append_bf16`` -- pinned: every row placed by hand with numpy indexing
+  (K and V pools, first / middle / last slot, padding and past-the-pool slots
+  write nothing, every other element keeps its fill).
 * ``kv_page_tag_check`` -- pinned: hand-derived cases in ``tests/golden``,
   brute force, tag bump and 32-bit wrap-around.
 * ``kv_calibrate_scales`` -- pinned: numpy's max of |x| and IEEE float32

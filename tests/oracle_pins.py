@@ -178,6 +178,39 @@ def pin_append_placement(orc):
     assert np.array_equal(k_cache, k_ref) and np.array_equal(v_cache, v_ref)
 
 
+def pin_append_bf16_placement(orc):
+    """The BF16 cache stores each new token's bf16 bits unchanged at
+    [page][head][offset]: K rows in the K pool, V rows in the V pool; padding
+    slots (< 0) and slots past the pool write nothing; every other byte keeps
+    its fill.  Expected pools are placed by hand with numpy indexing."""
+    P, Hkv, S, D = 5, 3, 32, 128
+    rng = np.random.default_rng(6)
+    fill_k, fill_v = np.uint16(0xA5A5), np.uint16(0x5A5A)
+    k_cache = np.full((P, Hkv, S, D), fill_k, dtype=np.uint16)
+    v_cache = np.full((P, Hkv, S, D), fill_v, dtype=np.uint16)
+    # first and last slot of the pool, a slot in the middle, padding, past the pool
+    slots = np.array([0, 2 * S + 19, -7, P * S - 1, P * S, 4 * S + 1], dtype=np.int64)
+    n = slots.size
+    kb = bf16_bits((rng.standard_normal((n, Hkv, D)) * 5).astype(np.float32))
+    vb = bf16_bits((rng.standard_normal((n, Hkv, D)) * 5).astype(np.float32))
+    orc.kv_append_bf16(kb, vb, slots, k_cache, v_cache)
+    k_ref = np.full_like(k_cache, fill_k)
+    v_ref = np.full_like(v_cache, fill_v)
+    written = 0
+    for j, slot in enumerate(slots):
+        if slot < 0 or slot >= P * S:
+            continue
+        p, off = int(slot) // S, int(slot) % S
+        k_ref[p, :, off, :] = kb[j]
+        v_ref[p, :, off, :] = vb[j]
+        written += 1
+    assert written == 4
+    assert np.array_equal(k_cache, k_ref), "K rows land at [page][head][offset] of the K pool"
+    assert np.array_equal(v_cache, v_ref), "V rows land at [page][head][offset] of the V pool"
+    # the bf16 bits round-trip: the cache holds exactly the input values
+    assert np.array_equal(bits_to_f32(k_cache[2, 1, 19]), bits_to_f32(kb[1, 1]))
+
+
 def pin_append_saturates(orc):
     P, Hkv, S, D = 1, 1, 16, 128
     k = np.zeros((P, Hkv, S, D), np.uint8)

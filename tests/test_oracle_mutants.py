@@ -24,7 +24,31 @@ MUTANTS = {
                             "                float kx",
                             "int64_t dst = (((page * num_kv_heads) + h) * page_size + (page_size - 1 - off)) * head_dim + d;\n"
                             "                float kx"),
-    "append_v_uses_k_scale": ("oracle_div_rn_f32(vx, v_scale[h])", "oracle_div_rn_f32(vx, k_scale[h])"),
+    "append_bf16_wrong_offset": ("int64_t dst = (((page * num_kv_heads) + h) * page_size + off) * head_dim + d;\n"
+                                 "                k_cache[dst] = k_new[src];",
+                                 "int64_t dst = (((page * num_kv_heads) + h) * page_size + (page_size - 1 - off)) * head_dim + d;\n"
+                                 "                k_cache[dst] = k_new[src];"),
+    "append_bf16_kv_swapped": ("k_cache[dst] = k_new[src];\n                v_cache[dst] = v_new[src];",
+                               "k_cache[dst] = v_new[src];\n                v_cache[dst] = k_new[src];"),
+    "append_bf16_head_stride": ("int64_t src = ((int64_t)n * num_kv_heads + h) * head_dim + d;\n"
+                                "                int64_t dst = (((page * num_kv_heads) + h) * page_size + off) * head_dim + d;\n"
+                                "                k_cache[dst]",
+                                "int64_t src = ((int64_t)n * num_kv_heads + (num_kv_heads - 1 - h)) * head_dim + d;\n"
+                                "                int64_t dst = (((page * num_kv_heads) + h) * page_size + off) * head_dim + d;\n"
+                                "                k_cache[dst]"),
+    "append_bf16_writes_past_pool": ("        if (page >= num_pages)\n            continue;\n"
+                                     "        for (int32_t h = 0; h < num_kv_heads; ++h) {\n"
+                                     "            for (int32_t d = 0; d < head_dim; ++d) {\n"
+                                     "                int64_t src = ((int64_t)n * num_kv_heads + h) * head_dim + d;\n"
+                                     "                int64_t dst = (((page * num_kv_heads) + h) * page_size + off) * head_dim + d;\n"
+                                     "                k_cache[dst]",
+                                     "        if (page >= num_pages)\n            page = num_pages - 1;\n"
+                                     "        for (int32_t h = 0; h < num_kv_heads; ++h) {\n"
+                                     "            for (int32_t d = 0; d < head_dim; ++d) {\n"
+                                     "                int64_t src = ((int64_t)n * num_kv_heads + h) * head_dim + d;\n"
+                                     "                int64_t dst = (((page * num_kv_heads) + h) * page_size + off) * head_dim + d;\n"
+                                     "                k_cache[dst]"),
+    "append_v_uses_k_scale":("oracle_div_rn_f32(vx, v_scale[h])", "oracle_div_rn_f32(vx, k_scale[h])"),
     "tag_compare_inverted": ("if (page_tags[page] != expected_tags[j]) {", "if (page_tags[page] == expected_tags[j]) {"),
     "tag_no_range_check": ("if (page < 0 || page >= num_pages) {\n                abort_r = 1;",
                            "if (0) {\n                abort_r = 1;"),
