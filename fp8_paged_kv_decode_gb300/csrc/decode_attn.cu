@@ -1375,7 +1375,14 @@ namespace {
 
 constexpr int kMaxDev = 64;
 std::mutex g_mu;
-int g_ctas_per_sm[kMaxDev][2][2];    // [dev][kv_fp8][ws]
+// Resident CTAs per SM, [dev][kv_fp8][ws], with the id of the context in
+// which the kernels' shared-memory limit was raised: a new context (after
+// cudaDeviceReset) loads the kernels again, so the attribute is set again.
+struct CtasPerSm {
+    unsigned long long ctx_id;
+    int n;
+};
+CtasPerSm g_ctas_per_sm[kMaxDev][2][2];
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1396,8 +1403,9 @@ int ctas_per_sm() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
     std::lock_guard<std::mutex> lk(g_mu);
-    int &v = g_ctas_per_sm[dev][kFp8 ? 1 : 0][kWS ? 1 : 0];
-    if (!v) {
+    CtasPerSm &c = g_ctas_per_sm[dev][kFp8 ? 1 : 0][kWS ? 1 : 0];
+    const unsigned long long ctx = current_context_id();
+    if (!c.n || ctx == 0 || ctx != c.ctx_id) {
         const int smem = Layout<kFp8>::kSmem;
         if (cudaFuncSetAttribute(paged_decode_attn_kernel<kFp8, kWS, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
@@ -1409,9 +1417,10 @@ int ctas_per_sm() {
                                                           attn_threads(kWS), smem) != cudaSuccess ||
             nb <= 0)
             return 0;
-        v = nb < 16 ? nb : 16;
+        c.n = nb < 16 ? nb : 16;
+        c.ctx_id = current_context_id();
     }
-    return v;
+    return c.n;
 }
 
 // Computing warps of one launch (one per CTA).

@@ -28,20 +28,30 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
+CachedSymbol g_scratch[kMaxDevices];
 
-// Device address of the scratch array on the current device; looked up once
-// per device, the first time this entry point runs there.
+// Device address of the scratch array on the current device.  It is looked
+// up (cudaGetSymbolAddress, with the device current) the first time this
+// entry point runs in a context and kept with that context's id; when the
+// context changes -- cudaDeviceReset, or a primary context released and
+// created again, after which the library's device code is loaded anew and
+// the array may sit elsewhere -- the old address is dropped and looked up
+// again.
 void *scratch_for_current_device() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return nullptr;
-        g_scratch_ptr[dev] = ptr;
-    }
-    return g_scratch_ptr[dev];
+    CachedSymbol &c = g_scratch[dev];
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0 && ctx == c.ctx_id && c.ptr) return c.ptr;
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return nullptr;
+    c.ptr = ptr;
+    // Read after the lookup, which makes the primary context current if
+    // nothing had; an id of 0 is never matched, so the address is then
+    // looked up on every call.
+    c.ctx_id = current_context_id();
+    return ptr;
 }
 
 }  // namespace

@@ -1,5 +1,7 @@
 // fkv_api.cu -- library-wide host helpers: status strings, the sticky device
 // error word, cached device properties.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 #include <string>
 
@@ -13,7 +15,7 @@ __device__ uint32_t g_device_error;
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-uint32_t *g_err_ptr[kMaxDevices] = {};
+CachedSymbol g_err_word[kMaxDevices];
 int g_sm_count[kMaxDevices] = {};
 
 int current_device() {
@@ -21,18 +23,47 @@ int current_device() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
     return dev;
 }
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
+std::once_flag g_ctx_fns_once;
 }  // namespace
+
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_fns_once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    });
+    if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 uint32_t *device_error_word() {
     const int dev = current_device();
     if (dev < 0) return nullptr;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_err_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-        g_err_ptr[dev] = static_cast<uint32_t *>(p);
-    }
-    return g_err_ptr[dev];
+    CachedSymbol &c = g_err_word[dev];
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0 && ctx == c.ctx_id && c.ptr) return static_cast<uint32_t *>(c.ptr);
+    // First use in this context, or a new context: look the address up again.
+    // cudaGetSymbolAddress makes the primary context current if nothing had,
+    // so the id is read after it (0: not cached, looked up on every call).
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess || !p) return nullptr;
+    c.ptr = p;
+    c.ctx_id = current_context_id();
+    return static_cast<uint32_t *>(p);
 }
 
 int device_sm_count() {

@@ -18,6 +18,17 @@ namespace fkv {
 // host side helpers (defined in fkv_api.cu)
 // ---------------------------------------------------------------------------
 uint32_t *device_error_word();           // sticky error word of the current device
+// Driver-assigned id of the calling thread's current CUDA context, 0 when
+// there is none.  The driver never reuses an id within a process, so a
+// context torn down by cudaDeviceReset and created again has a new id even
+// if it sits at the same address; device addresses of __device__ variables
+// cached per context are keyed by it.
+unsigned long long current_context_id();
+// A cached device address and the id of the context it was looked up in.
+struct CachedSymbol {
+    unsigned long long ctx_id = 0;
+    void *ptr = nullptr;
+};
 int device_sm_count();                   // SMs of the current device
 bool aligned16(const void *p);
 

@@ -261,7 +261,12 @@ FKV_API fkv_status paged_decode_attn(const void *q, int32_t batch, int32_t num_q
  *     roughly batch * num_kv_heads up to 3000 on a 152-SM GB300.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept together with the id
+ *     of the CUDA context it was found in.  When the context changes --
+ *     cudaDeviceReset, or the primary context released and created again,
+ *     which loads the library's device code anew -- the kept address is
+ *     dropped and the next call looks it up again (so that call, too, is a
+ *     first call and belongs outside stream capture).
  *   - All calls on a device share the one array and it keeps whatever the
  *     last call left in it (each call clears what it needs cleared).  Calls
  *     that overlap on the GPU -- on different streams, or from different host

@@ -1,14 +1,22 @@
-"""The no-allocation attention entry point against the regular one (GPU).
+"""The no-allocation attention entry point (GPU).
 
 paged_decode_attn_noalloc serves callers that cannot allocate device memory
 (a plugin whose host runtime owns every allocation and passes it only its
 inputs and outputs, or a serving loop that forbids cudaMalloc on its hot path
 because it can synchronise the device).  It keeps its scratch in a fixed
-array inside the library.  Here it is called through the C ABI twice in a
-row, on two different batches, and each output is checked against
-paged_decode_attn on the same inputs within the tolerance used by every
-attention test.  The file is named so pytest collects it last.
+array inside the library.
+
+Here it is called through the package's ctypes binding, which hands the
+tensors' device pointers straight to the C entry point, several times in a
+row on different batches.  Each output is checked against the CPU oracle
+and against paged_decode_attn on the same inputs, within the tolerance used
+by every attention test.  A plain C program then drives the entry point
+through the C ABI alone, across a cudaDeviceReset, and checks it against the
+C oracle.  The file is named so pytest collects it last.
 """
+import os
+import subprocess
+
 import numpy as np
 import pytest
 
@@ -38,10 +46,37 @@ def test_noalloc_matches_regular_entry_point_twice(orc, kv):
     first = PagedCase(orc, 6, 64, 8, 64, [40000, 17, 3000, 1, 9000, 640], kv=kv, seed=501)
     second = PagedCase(orc, 4, 32, 8, 16, [4097, 33, 2, 1500], kv=kv, seed=502)
     third = PagedCase(orc, 3, 32, 2, 64, [5000, 40, 2100], kv=kv, seed=503)   # 16 query heads per KV head
-    for case in (first, second, third):              # calls in a row share the scratch
-        want = bf16_out(case.gpu())                  # regular entry point, caller-provided workspace
+    cases = (first, second, third)
+    refs = [case.oracle(orc) for case in cases]
+    for case, ref in zip(cases, refs):               # calls in a row share the scratch
         got = bf16_out(_noalloc(case))
+        assert_close(got, ref, "noalloc vs oracle (%s, B=%d)" % (kv, case.B))
+        want = bf16_out(case.gpu())                  # regular entry point, caller-provided workspace
         assert_close(got, want, "noalloc vs regular (%s, B=%d)" % (kv, case.B))
+        assert_close(want, ref, "regular vs oracle (%s, B=%d)" % (kv, case.B))
+
+
+def test_noalloc_c_abi_across_device_reset(tmp_path):
+    """Plain C, no torch: two calls in a row, then cudaDeviceReset (a new
+    context, in which the library looks its scratch address up again), then a
+    third call; all checked against the C oracle."""
+    import fp8_paged_kv_decode_gb300 as fkv
+    from test_gpu_c_abi import ROOT, HERE, _cuda_home
+    lib = fkv.library_path()
+    assert os.path.exists(lib), "libfkv.so is not built"
+    cuda = _cuda_home()
+    assert cuda, "CUDA toolkit not found"
+    libdir = os.path.dirname(lib)
+    exe = str(tmp_path / "c_abi_noalloc")
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                    "-I", os.path.join(ROOT, "include"), "-I", os.path.join(cuda, "include"),
+                    os.path.join(HERE, "c_abi_noalloc.c"), os.path.join(ROOT, "oracle", "fkv_oracle.c"),
+                    "-o", exe, "-L", libdir, "-l:" + os.path.basename(lib),
+                    "-L", os.path.join(cuda, "lib64"), "-lcudart", "-lm", "-Wl,-rpath," + libdir],
+                   check=True)
+    res = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stdout + res.stderr
+    assert "c abi noalloc ok" in res.stdout, res.stdout
 
 
 def test_workspace_of_a_split_group():
