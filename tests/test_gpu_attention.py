@@ -45,6 +45,37 @@ def test_peaky_softmax(orc):
     assert_close(bf16_out(case.gpu()), case.oracle(orc), "peaky")
 
 
+def wide_range_q(case, mults, seed, zero_k=False):
+    """Scale a few channels of every query head by large factors (the other
+    channels stay N(0,1)), so one query row spans a wide dynamic range.  The
+    channels are chosen per KV head and shared by its query heads; with
+    ``zero_k`` the K codes of those channels are zero in the whole pool, so the
+    large channels add nothing to the logits and the small ones decide them."""
+    rng = np.random.default_rng(seed)
+    G = case.Hq // case.Hkv
+    q = W.bits_to_f32(case.q).copy()
+    for h in range(case.Hkv):
+        ch = rng.choice(case.D, size=len(mults), replace=False)
+        for c, m in zip(ch, mults):
+            q[:, h * G:(h + 1) * G, c] *= np.float32(m)
+        if zero_k:
+            case.kc[:, h, :, ch] = 0
+    case.q = W.bf16_bits(q)
+
+
+@pytest.mark.parametrize("zero_k", [False, True], ids=["k_random", "k_zero_in_large_channels"])
+@pytest.mark.parametrize("G", [4, 8])
+def test_wide_dynamic_range_q(orc, G, zero_k):
+    """FP8 KV: the queries enter the tensor cores as f16 with a power-of-two
+    scale per row; a row whose channels span 1 to 1e4 (three channels x1e3,
+    x1e4, x1e4) still matches the oracle, with K random in those channels
+    (a very peaky softmax) or zero there (the small channels decide)."""
+    Hkv = 2
+    case = PagedCase(orc, 4, G * Hkv, Hkv, 64 if G == 8 else 16, [3000, 100, 17, 800], seed=60 + G + zero_k)
+    wide_range_q(case, [1e3, 1e4, 1e4], seed=70 + G, zero_k=zero_k)
+    assert_close(bf16_out(case.gpu()), case.oracle(orc), "G=%d zero_k=%s" % (G, zero_k))
+
+
 @pytest.mark.parametrize("S", [16, 64])
 def test_fail_closed_rows(orc, S):
     """Aborted, empty, over-long and bad-page requests give zero rows; the

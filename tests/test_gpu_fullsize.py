@@ -1,10 +1,16 @@
 """The five workloads at full size, through the same calls and launch
-configuration the benchmark times.  The oracle checks sampled requests (all
-their query heads) rebuilt from the bf16 source values it encodes itself;
-properties that hold at any size are checked on every row."""
+configuration the benchmark times, checked against the oracle on the whole
+batch: the oracle encodes every cached token and the step's token itself from
+the bf16 source values (drawn by torch's generator), and every byte of both
+pools must equal the GPU's; the abort mask is compared for every request; and
+every (request, query head) row of the attention output is compared element
+by element within the tolerance, aborted rows exactly zero.  The oracle's work
+is split over the host's threads (tokens for the encode, rows for attention);
+the split changes none of its arithmetic."""
 import numpy as np
 import pytest
 
+import oracle_parallel as OP
 from fp8_paged_kv_decode_gb300 import workloads as W
 from gpu_util import assert_close, bf16_out, dev
 
@@ -45,70 +51,61 @@ def run_step(db, kv):
     return k_cache, v_cache, mask, out
 
 
-def sample_requests(db, mask, n=3):
-    live = np.nonzero(mask == 0)[0]
-    dead = np.nonzero(mask != 0)[0]
-    pick = []
-    if live.size:
-        pick += [int(live[np.argmax(db.seq_lens[live])]), int(live[np.argmin(db.seq_lens[live])])]
-        rng = np.random.default_rng(0)
-        pick += [int(x) for x in rng.choice(live, size=min(n - 2, live.size), replace=False)]
-    if dead.size:
-        pick.append(int(dead[0]))
-    return np.unique(pick)
+def _host_u16(t):
+    """bf16 device tensor -> numpy uint16 bit patterns (a copy, no arithmetic)."""
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _assert_pool_equal(got, want, what):
+    if not np.array_equal(got, want):
+        bad = np.flatnonzero(got.reshape(-1) != want.reshape(-1))
+        idx = np.unravel_index(bad[0], want.shape)
+        raise AssertionError("%s: %d of %d elements differ from the oracle; first at [page %d][head %d][slot %d]"
+                             "[dim %d]: got %#x want %#x" % (what, bad.size, want.size, *idx,
+                                                             int(got[idx]), int(want[idx])))
 
 
 @pytest.mark.parametrize("name,kv", CASES, ids=["%s-%s" % c for c in CASES])
-def test_fullsize_sampled_parity(orc, name, kv):
+def test_fullsize_whole_batch_parity(orc, name, kv):
     import torch
     import fp8_paged_kv_decode_gb300 as fkv
     wl = W.WORKLOADS[name]
     fkv.device_error(clear=True)
     db = W.device_batch(wl, "cuda")
     k_cache, v_cache, mask, out = run_step(db, kv)
-    mask_np = mask.cpu().numpy()
+    fp8 = kv == "fp8"
     # the abort mask over the whole batch is bit-exact
     want_mask = orc.kv_page_tag_check(db.pt.page_tags, db.pt.indptr, db.pt.indices, db.pt.expected_tags)
-    assert np.array_equal(mask_np, want_mask)
+    assert np.array_equal(mask.cpu().numpy(), want_mask)
     assert (want_mask.sum() > 0) == (wl.stale_frac > 0)
-    got_all = out.float()
-    # properties on every row: finite; aborted rows exactly zero
-    assert torch.isfinite(got_all).all()
-    if want_mask.any():
-        assert not got_all[torch.from_numpy(want_mask.astype(bool)).cuda()].abs().sum().item()
-    # sampled requests against the oracle
-    reqs = sample_requests(db, want_mask)
-    cr = W.compact_requests(db, reqs)
-    P2, Hkv, S, D = cr.num_pages, wl.num_kv_heads, wl.page_size, wl.head_dim
-    if kv == "fp8":
-        kc = np.zeros((P2, Hkv, S, D), np.uint8)
-        vc = np.zeros((P2, Hkv, S, D), np.uint8)
-        orc.kv_append_fp8(cr.k_tokens, cr.v_tokens, cr.slots, db.k_scale, db.v_scale, kc, vc)
-        gk = k_cache[torch.from_numpy(cr.orig_pages).cuda()].cpu().numpy()
-        gv = v_cache[torch.from_numpy(cr.orig_pages).cuda()].cpu().numpy()
+
+    # the oracle's pools: every cached token and the step's token, encoded by the oracle
+    P, Hkv, S, D = db.pt.num_pages, wl.num_kv_heads, wl.page_size, wl.head_dim
+    slots = np.concatenate([db.slots_src.cpu().numpy(), db.slots_new.cpu().numpy()])
+    k_tok = np.concatenate([_host_u16(db.k_src), _host_u16(db.k_new)])
+    v_tok = np.concatenate([_host_u16(db.v_src), _host_u16(db.v_new)])
+    if fp8:
+        kc = np.zeros((P, Hkv, S, D), np.uint8)
+        vc = np.zeros((P, Hkv, S, D), np.uint8)
+        OP.append_fp8(orc, k_tok, v_tok, slots, db.k_scale, db.v_scale, kc, vc)
     else:
-        kc = np.zeros((P2, Hkv, S, D), np.uint16)
-        vc = np.zeros((P2, Hkv, S, D), np.uint16)
-        orc.kv_append_bf16(cr.k_tokens, cr.v_tokens, cr.slots, kc, vc)
-        pages = torch.from_numpy(cr.orig_pages).cuda()
-        gk = k_cache[pages].view(torch.int16).cpu().numpy().view(np.uint16)
-        gv = v_cache[pages].view(torch.int16).cpu().numpy().view(np.uint16)
-    # the appended bytes of every sampled token slot are bit-exact
-    pg, off = cr.slots // S, cr.slots % S
-    assert np.array_equal(gk[pg, :, off], kc[pg, :, off]) and np.array_equal(gv[pg, :, off], vc[pg, :, off])
-    # every head of short requests; 8 heads spread over the KV heads of long ones
-    Hq, G = wl.num_q_heads, wl.group
-    rows = []
-    for j, r in enumerate(cr.reqs):
-        heads = range(Hq) if db.seq_lens[r] <= 16384 else [k * (Hq // 8) + (k % (Hq // 8)) for k in range(8)]
-        rows += [j * Hq + i for i in heads]
-    rows = np.array(rows, np.int32)
-    ref = orc.paged_decode_attn(cr.q, kc, vc, cr.indptr, cr.indices, cr.seq_lens, 1.0 / np.sqrt(D),
-                                k_scale=db.k_scale if kv == "fp8" else None,
-                                v_scale=db.v_scale if kv == "fp8" else None,
-                                abort_mask=want_mask[cr.reqs], rows=rows)
-    got = bf16_out(out[torch.from_numpy(cr.reqs).cuda()]).reshape(-1, D)[rows]
-    assert_close(got, ref, "%s %s requests %s" % (name, kv, cr.reqs.tolist()))
+        kc = np.zeros((P, Hkv, S, D), np.uint16)
+        vc = np.zeros((P, Hkv, S, D), np.uint16)
+        OP.append_bf16(orc, k_tok, v_tok, slots, kc, vc)
+    del k_tok, v_tok
+    # every byte of both pools (written slots and untouched ones) equals the oracle's
+    _assert_pool_equal(k_cache.cpu().numpy() if fp8 else _host_u16(k_cache), kc, "%s %s K pool" % (name, kv))
+    _assert_pool_equal(v_cache.cpu().numpy() if fp8 else _host_u16(v_cache), vc, "%s %s V pool" % (name, kv))
+
+    # every row of the attention output
+    ref = OP.attention_rows(orc, _host_u16(db.q), kc, vc, db.pt.indptr, db.pt.indices, db.seq_lens,
+                            1.0 / np.sqrt(D), k_scale=db.k_scale if fp8 else None,
+                            v_scale=db.v_scale if fp8 else None, abort_mask=want_mask)
+    got = bf16_out(out)
+    assert np.isfinite(got).all()
+    assert not got[want_mask.astype(bool)].any(), "aborted rows must be exactly zero"
+    assert_close(got, ref, "%s %s, all %d rows" % (name, kv, wl.batch * wl.num_q_heads))
     assert fkv.device_error() == 0
 
 
