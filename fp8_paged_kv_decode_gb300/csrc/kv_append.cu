@@ -13,7 +13,7 @@
 // work is tiny (one token per request); for a bulk prefill write it is plain
 // bandwidth, provided the arithmetic per element stays small -- hence the
 // division below.
-#include "fkv_common.cuh"
+#include "tag_check_row.cuh"
 
 namespace fkv {
 
@@ -68,11 +68,11 @@ __device__ __forceinline__ bool recip_scale_ok(float b) {
 
 // Token of this thread (or -1: nothing to write) and the element offset of
 // its (slot, head) row in the pool; the thread's part of the row starts
-// chunk * 16 elements further on.
+// chunk * 16 elements further on.  (bx, by) = (16-token group, KV head).
 __device__ __forceinline__ int64_t locate(const int64_t *__restrict__ slots, int64_t n_tokens, int32_t num_pages,
                                           int32_t num_kv_heads, int32_t page_size, int32_t page_shift,
-                                          uint32_t *err, int64_t &offset_elems) {
-    const int64_t n = static_cast<int64_t>(blockIdx.x) * kTokensPerBlock + (threadIdx.x / kThreadsPerToken);
+                                          uint32_t *err, unsigned bx, unsigned by, int64_t &offset_elems) {
+    const int64_t n = static_cast<int64_t>(bx) * kTokensPerBlock + (threadIdx.x / kThreadsPerToken);
     if (n >= n_tokens) return -1;
     const int64_t slot = __ldg(slots + n);
     if (slot < 0) return -1;                                      // padding token
@@ -82,23 +82,21 @@ __device__ __forceinline__ int64_t locate(const int64_t *__restrict__ slots, int
         if ((threadIdx.x % kThreadsPerToken) == 0) atomicOr(err, FKV_DEVERR_APPEND_SLOT);
         return -1;
     }
-    offset_elems = ((page * num_kv_heads + blockIdx.y) * page_size + off) * kHeadDim;
+    offset_elems = ((page * num_kv_heads + by) * page_size + off) * kHeadDim;
     return n;
 }
 
-__global__ void __launch_bounds__(kBlock, FKV_APPEND_MIN_BLOCKS)
-kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
-                     const int64_t *__restrict__ slots, int64_t n_tokens,
-                     const float *__restrict__ k_scale, const float *__restrict__ v_scale,
-                     uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
-                     int32_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t page_shift,
-                     uint32_t *err) {
-    grid_dep_wait();        // earlier readers of the pool (attention) have finished
-    grid_dep_launch();
+// One thread's share of the FP8 append in block (bx, by).
+__device__ __forceinline__ void append_fp8_part(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                                                const int64_t *__restrict__ slots, int64_t n_tokens,
+                                                const float *__restrict__ k_scale, const float *__restrict__ v_scale,
+                                                uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
+                                                int32_t num_pages, int32_t num_kv_heads, int32_t page_size,
+                                                int32_t page_shift, uint32_t *err, unsigned bx, unsigned by) {
     int64_t dst_off = 0;
-    const int64_t n = locate(slots, n_tokens, num_pages, num_kv_heads, page_size, page_shift, err, dst_off);
+    const int64_t n = locate(slots, n_tokens, num_pages, num_kv_heads, page_size, page_shift, err, bx, by, dst_off);
     if (n < 0) return;
-    const int h = blockIdx.y;
+    const int h = by;
     const int sub = threadIdx.x % kThreadsPerToken;
     const bool is_v = sub >= kThreadsPerRow;
     const int chunk = sub % kThreadsPerRow;
@@ -143,6 +141,51 @@ kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ 
     __stcs(reinterpret_cast<uint4 *>(dst), make_uint4(packed[0], packed[1], packed[2], packed[3]));
 }
 
+__global__ void __launch_bounds__(kBlock, FKV_APPEND_MIN_BLOCKS)
+kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                     const int64_t *__restrict__ slots, int64_t n_tokens,
+                     const float *__restrict__ k_scale, const float *__restrict__ v_scale,
+                     uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
+                     int32_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t page_shift,
+                     uint32_t *err) {
+    grid_dep_wait();        // earlier readers of the pool (attention) have finished
+    grid_dep_launch();
+    append_fp8_part(k_new, v_new, slots, n_tokens, k_scale, v_scale, k_cache, v_cache, num_pages, num_kv_heads,
+                    page_size, page_shift, err, blockIdx.x, blockIdx.y);
+}
+
+// The decode step's append and the integrity check in one launch.  The two
+// touch disjoint memory -- the append writes cache bytes only, the check
+// reads tags and page tables and writes the abort mask -- so running them
+// side by side gives exactly the bytes and the mask of kv_append_fp8
+// followed by kv_page_tag_check, and the check still runs as its own pass
+// before attention, outside the attention kernel.  Blocks [0, batch) check
+// one request each; the rest are the append's (16-token group, KV head)
+// blocks in x-major order.
+__global__ void __launch_bounds__(kBlock, FKV_APPEND_MIN_BLOCKS)
+kv_append_fp8_tag_check_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                               const int64_t *__restrict__ slots, int64_t n_tokens,
+                               const float *__restrict__ k_scale, const float *__restrict__ v_scale,
+                               uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
+                               int32_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t page_shift,
+                               uint32_t *err, unsigned append_blocks_x,
+                               const uint32_t *__restrict__ page_tags, const int32_t *__restrict__ page_indptr,
+                               const int32_t *__restrict__ page_indices, const uint32_t *__restrict__ expected_tags,
+                               int32_t batch, int64_t nnz, uint8_t *__restrict__ abort_mask) {
+    grid_dep_wait();        // earlier kernels' tags, tables and pool readers are done
+    grid_dep_launch();
+    const unsigned b = blockIdx.x;
+    if (b < static_cast<unsigned>(batch)) {
+        const int bad = tag_check_row<kBlock>(page_tags, num_pages, page_indptr, page_indices, expected_tags, nnz,
+                                              static_cast<int>(b));
+        if (threadIdx.x == 0) abort_mask[b] = bad ? 1 : 0;
+        return;
+    }
+    const unsigned a = b - static_cast<unsigned>(batch);
+    append_fp8_part(k_new, v_new, slots, n_tokens, k_scale, v_scale, k_cache, v_cache, num_pages, num_kv_heads,
+                    page_size, page_shift, err, a % append_blocks_x, a / append_blocks_x);
+}
+
 __global__ void __launch_bounds__(kBlock)
 kv_append_bf16_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                       const int64_t *__restrict__ slots, int64_t n_tokens,
@@ -152,7 +195,8 @@ kv_append_bf16_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__
     grid_dep_wait();        // earlier readers of the pool (attention) have finished
     grid_dep_launch();
     int64_t dst_off = 0;
-    const int64_t n = locate(slots, n_tokens, num_pages, num_kv_heads, page_size, page_shift, err, dst_off);
+    const int64_t n = locate(slots, n_tokens, num_pages, num_kv_heads, page_size, page_shift, err, blockIdx.x,
+                             blockIdx.y, dst_off);
     if (n < 0) return;
     const int h = blockIdx.y;
     const int sub = threadIdx.x % kThreadsPerToken;
@@ -229,5 +273,38 @@ extern "C" fkv_status kv_append_bf16(const void *k_new, const void *v_new, const
                                      static_cast<const uint4 *>(v_new), slot_mapping, static_cast<int64_t>(n_tokens),
                                      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_pages,
                                      num_kv_heads, page_size, page_shift_of(page_size), err);
+    return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
+}
+
+extern "C" fkv_status kv_append_fp8_tag_check(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                                              int32_t n_tokens, const float *k_scale, const float *v_scale,
+                                              uint8_t *k_cache, uint8_t *v_cache, int32_t num_pages,
+                                              int32_t num_kv_heads, int32_t page_size, int32_t head_dim,
+                                              const uint32_t *page_tags, const int32_t *page_indptr,
+                                              const int32_t *page_indices, const uint32_t *expected_tags,
+                                              int32_t batch, int64_t nnz, uint8_t *abort_mask, void *stream) {
+    fkv_status st = check_append_args(k_new, v_new, slot_mapping, n_tokens, k_cache, v_cache, num_pages,
+                                      num_kv_heads, page_size, head_dim);
+    if (st != FKV_OK) return st;
+    if (n_tokens > 0 && (!k_scale || !v_scale)) return FKV_ERR_INVALID_ARG;
+    // the check's arguments, as kv_page_tag_check takes them
+    if (batch < 0 || nnz < 0) return FKV_ERR_INVALID_ARG;
+    if (batch > 0) {
+        if (!page_indptr || !abort_mask || !page_tags) return FKV_ERR_INVALID_ARG;
+        if (nnz > 0 && (!page_indices || !expected_tags)) return FKV_ERR_INVALID_ARG;
+    }
+    if (n_tokens == 0 && batch == 0) return FKV_OK;
+    const int64_t gx = (static_cast<int64_t>(n_tokens) + kTokensPerBlock - 1) / kTokensPerBlock;
+    const int64_t blocks = gx * num_kv_heads + batch;
+    if (blocks > 0x7FFFFFFF) return FKV_ERR_UNSUPPORTED;
+    uint32_t *err = device_error_word();
+    if (!err) return FKV_ERR_CUDA;
+    const cudaError_t e = launch_pdl(kv_append_fp8_tag_check_kernel, dim3(static_cast<unsigned>(blocks)),
+                                     dim3(kBlock), 0, static_cast<cudaStream_t>(stream),
+                                     static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+                                     slot_mapping, static_cast<int64_t>(n_tokens), k_scale, v_scale, k_cache,
+                                     v_cache, num_pages, num_kv_heads, page_size, page_shift_of(page_size), err,
+                                     static_cast<unsigned>(gx > 0 ? gx : 1), page_tags, page_indptr, page_indices,
+                                     expected_tags, batch, nnz, abort_mask);
     return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
 }

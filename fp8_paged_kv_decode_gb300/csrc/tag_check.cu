@@ -9,11 +9,9 @@
 // as a separate batch pass, not fused into the attention kernel; this file is
 // that pass.
 //
-// One CTA per request: its threads stride over the request's CSR row,
-// gathering the live tag of each listed page (the tag array is small and stays
-// in L2), and the CTA ORs the per-thread verdicts with __syncthreads_or.  The
-// abort mask stays on the device for the attention call.
-#include "fkv_common.cuh"
+// One CTA per request (tag_check_row.cuh); the abort mask stays on the
+// device for the attention call.
+#include "tag_check_row.cuh"
 
 namespace fkv {
 
@@ -27,36 +25,8 @@ kv_page_tag_check_kernel(const uint32_t *__restrict__ page_tags, int32_t num_pag
     grid_dep_wait();        // tags and tables written by earlier kernels are visible
     grid_dep_launch();
     const int r = blockIdx.x;
-    const int64_t begin = __ldg(page_indptr + r);
-    const int64_t end = __ldg(page_indptr + r + 1);
-    int bad = 0;
-    if (begin < 0 || end < begin || end > nnz) {
-        bad = 1;                                            // malformed row: fail closed
-    } else {
-        int64_t j = begin + threadIdx.x;
-        // four independent gathers in flight per thread
-        for (; j + 3 * kCheckThreads < end; j += 4 * kCheckThreads) {
-            int32_t p[4];
-            uint32_t e[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                p[u] = __ldg(page_indices + j + u * kCheckThreads);
-                e[u] = __ldg(expected_tags + j + u * kCheckThreads);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (p[u] < 0 || p[u] >= num_pages) bad = 1;        // no such page
-                else bad |= __ldg(page_tags + p[u]) != e[u];     // stale or mismatched
-            }
-        }
-        for (; j < end; j += kCheckThreads) {
-            const int32_t p = __ldg(page_indices + j);
-            const uint32_t e = __ldg(expected_tags + j);
-            if (p < 0 || p >= num_pages) bad = 1;
-            else bad |= __ldg(page_tags + p) != e;
-        }
-    }
-    bad = __syncthreads_or(bad);
+    const int bad = tag_check_row<kCheckThreads>(page_tags, num_pages, page_indptr, page_indices, expected_tags,
+                                                 nnz, r);
     if (threadIdx.x == 0) abort_mask[r] = bad ? 1 : 0;
 }
 

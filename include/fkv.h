@@ -158,6 +158,33 @@ FKV_API fkv_status kv_page_tag_check(const uint32_t *page_tags, int32_t num_page
                              uint8_t *abort_mask, void *stream);
 
 /*
+ * kv_append_fp8_tag_check -- kv_append_fp8 and kv_page_tag_check of one
+ * decode step in a single launch.  (Cloudflare post, integrity checking: the
+ * check runs as a separate batch pass before decode reads the cache, not
+ * inside the attention kernel; this call keeps it a pass of its own and only
+ * shares the append's launch.)
+ *
+ * Equivalent to kv_append_fp8(k_new ... head_dim) followed by
+ * kv_page_tag_check(page_tags, num_pages, page_indptr, page_indices,
+ * expected_tags, batch, nnz, abort_mask) on the same stream: the same cache
+ * bytes, the same mask, the same argument checks and error codes.  The two
+ * parts touch disjoint memory (the append writes only cache bytes, the check
+ * reads tags and tables and writes only abort_mask), so the kernel runs them
+ * side by side; the caller must not pass buffers that overlap across the two
+ * parts.  page_tags has num_pages entries (the pool the append writes into).
+ * n_tokens == 0 runs the check alone, batch == 0 the append alone.
+ */
+FKV_API fkv_status kv_append_fp8_tag_check(const void *k_new, const void *v_new,
+                                   const int64_t *slot_mapping, int32_t n_tokens,
+                                   const float *k_scale, const float *v_scale,
+                                   uint8_t *k_cache, uint8_t *v_cache,
+                                   int32_t num_pages, int32_t num_kv_heads,
+                                   int32_t page_size, int32_t head_dim,
+                                   const uint32_t *page_tags, const int32_t *page_indptr,
+                                   const int32_t *page_indices, const uint32_t *expected_tags,
+                                   int32_t batch, int64_t nnz, uint8_t *abort_mask, void *stream);
+
+/*
  * kv_page_realloc -- hand pages to new owners on the device ("Kimi and GLM
  * Reasoning Slimming: Hands-On Test", section "Giving Every Physical Cache
  * Page a 'Generation Number'": a page's tag changes each time it is

@@ -1,0 +1,115 @@
+"""kv_append_fp8_tag_check on the GPU: the decode step's append and the
+integrity check in one launch give the oracle's pool bytes and abort mask bit
+for bit, and exactly what the two separate calls give."""
+import numpy as np
+import pytest
+
+from fp8_paged_kv_decode_gb300 import workloads as W
+from gpu_util import dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _tables(rng, P, B, faults=True):
+    tags = rng.integers(0, 2 ** 32, P, dtype=np.uint64).astype(np.uint32)
+    counts = rng.integers(0, 300, B)
+    indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    nnz = int(indptr[-1])
+    indices = rng.integers(0, P, nnz).astype(np.int32)
+    expected = tags[indices].copy()
+    if faults and nnz:
+        j = rng.integers(0, nnz, max(1, nnz // 500))
+        expected[j[::2]] += np.uint32(1)                         # stale tags
+        indices[j[1::2]] = P + 3                                 # ids outside the pool
+    return tags, indptr, indices, expected
+
+
+def _run(orc, P, Hkv, S, N, B, seed, combined=True, faults=True):
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    rng = np.random.default_rng(seed)
+    kc0 = rng.integers(0, 256, (P, Hkv, S, 128)).astype(np.uint8)
+    vc0 = rng.integers(0, 256, (P, Hkv, S, 128)).astype(np.uint8)
+    slots = rng.choice(P * S, size=N, replace=False).astype(np.int64) if N else np.zeros(0, np.int64)
+    if N:
+        slots[::13] = -1                                         # padding tokens
+    kb = W.bf16_bits((rng.standard_normal((N, Hkv, 128)) * 3).astype(np.float32))
+    vb = W.bf16_bits(rng.standard_normal((N, Hkv, 128)).astype(np.float32))
+    ks = rng.uniform(0.002, 0.02, Hkv).astype(np.float32)
+    vs = rng.uniform(0.002, 0.02, Hkv).astype(np.float32)
+    tags, indptr, indices, expected = _tables(rng, P, B, faults)
+    # the oracle: append, then check
+    kc, vc = kc0.copy(), vc0.copy()
+    if N:
+        orc.kv_append_fp8(kb, vb, slots, ks, vs, kc, vc)
+    want_mask = orc.kv_page_tag_check(tags, indptr, indices, expected)
+    # the GPU
+    kt, vt = dev(kc0), dev(vc0)
+    mask = torch.full((B,), 7, dtype=torch.uint8, device="cuda")
+    args = (dev(kb, dtype=torch.bfloat16) if N else torch.zeros(0, Hkv, 128, dtype=torch.bfloat16, device="cuda"),
+            dev(vb, dtype=torch.bfloat16) if N else torch.zeros(0, Hkv, 128, dtype=torch.bfloat16, device="cuda"),
+            dev(slots) if N else torch.zeros(0, dtype=torch.int64, device="cuda"), dev(ks), dev(vs), kt, vt)
+    ind = dev(indices if indices.size else np.zeros(1, np.int32))[:indices.size]
+    exp = dev(expected.view(np.int32) if expected.size else np.zeros(1, np.int32))[:expected.size]
+    tg = dev(tags.view(np.int32))
+    fkv.device_error(clear=True)
+    if combined:
+        fkv.kv_append_fp8_tag_check(*args, tg, dev(indptr), ind, exp, mask)
+    else:
+        fkv.kv_append_fp8(*args)
+        fkv.kv_page_tag_check(tg, dev(indptr), ind, exp, mask)
+    torch.cuda.synchronize()
+    return kt.cpu().numpy(), vt.cpu().numpy(), mask.cpu().numpy(), kc, vc, want_mask
+
+
+@pytest.mark.parametrize("P,Hkv,S,N,B", [(300, 8, 16, 256, 256), (64, 2, 64, 37, 5), (2000, 4, 32, 1000, 900),
+                                         (50, 1, 128, 17, 1)])
+def test_combined_equals_oracle_and_separate_calls(orc, P, Hkv, S, N, B):
+    import fp8_paged_kv_decode_gb300 as fkv
+    seed = P + N + B
+    gk, gv, gm, kc, vc, want = _run(orc, P, Hkv, S, N, B, seed, combined=True)
+    assert np.array_equal(gk, kc) and np.array_equal(gv, vc), "pool bytes differ from the oracle"
+    assert np.array_equal(gm, want), "abort mask differs from the oracle"
+    assert want.any() or B == 1
+    sk, sv, sm, _, _, _ = _run(orc, P, Hkv, S, N, B, seed, combined=False)
+    assert np.array_equal(gk, sk) and np.array_equal(gv, sv) and np.array_equal(gm, sm)
+    assert fkv.device_error() == 0
+
+
+def test_check_only_and_append_only(orc):
+    """No tokens: the launch is the check alone.  An empty batch: the append alone."""
+    gk, gv, gm, kc, vc, want = _run(orc, 100, 2, 16, 0, 40, seed=9)
+    assert np.array_equal(gk, kc) and np.array_equal(gv, vc) and np.array_equal(gm, want)
+    gk, gv, gm, kc, vc, want = _run(orc, 100, 2, 16, 60, 0, seed=10)
+    assert np.array_equal(gk, kc) and np.array_equal(gv, vc) and gm.size == 0
+
+
+def test_integrity_workload_step(orc):
+    """The integrity workload's decode step: 256 appended tokens, 1% of pages
+    stale; the mask matches the oracle and the appended slots hold the
+    oracle's codes."""
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    wl = W.WORKLOADS["integrity_256req"]
+    rng = np.random.default_rng(wl.seed)
+    ctx = W.context_lengths(wl, rng)
+    pt = W.build_page_table(wl, ctx + 1, rng)
+    P, Hkv, S = pt.num_pages, wl.num_kv_heads, wl.page_size
+    kb = W.bf16_bits(rng.standard_normal((wl.batch, Hkv, 128)).astype(np.float32))
+    vb = W.bf16_bits(rng.standard_normal((wl.batch, Hkv, 128)).astype(np.float32))
+    slots = W.slot_mapping(pt, S, np.arange(wl.batch), ctx)
+    ks = np.full(Hkv, 0.01, np.float32)
+    vs = np.full(Hkv, 0.008, np.float32)
+    kt = torch.zeros(P, Hkv, S, 128, dtype=torch.uint8, device="cuda")
+    vt = torch.zeros_like(kt)
+    mask = torch.full((wl.batch,), 7, dtype=torch.uint8, device="cuda")
+    fkv.kv_append_fp8_tag_check(dev(kb, dtype=torch.bfloat16), dev(vb, dtype=torch.bfloat16), dev(slots), dev(ks),
+                                dev(vs), kt, vt, dev(pt.page_tags.view(np.int32)), dev(pt.indptr), dev(pt.indices),
+                                dev(pt.expected_tags.view(np.int32)), mask)
+    torch.cuda.synchronize()
+    want = orc.kv_page_tag_check(pt.page_tags, pt.indptr, pt.indices, pt.expected_tags)
+    assert np.array_equal(mask.cpu().numpy(), want) and 0 < want.sum() < wl.batch
+    kc = np.zeros((P, Hkv, S, 128), np.uint8)
+    vc = np.zeros_like(kc)
+    orc.kv_append_fp8(kb, vb, slots, ks, vs, kc, vc)
+    assert np.array_equal(kt.cpu().numpy(), kc) and np.array_equal(vt.cpu().numpy(), vc)
