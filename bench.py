@@ -63,6 +63,10 @@ def parse():
                     help="instead of the headline: requests sharing their first pages (a common prompt prefix)")
     ap.add_argument("--capacity-sweep", action="store_true",
                     help="instead of the headline: KV budget admission and a concurrency sweep, FP8 vs BF16")
+    ap.add_argument("--configs-only", action="store_true",
+                    help="instead of the headline: the attention call on every workload (the per-config table)")
+    ap.add_argument("--config-reps", type=int, default=None,
+                    help="timed attention calls per workload in the per-config table (default from --steps)")
     return ap.parse_args()
 
 
@@ -129,11 +133,9 @@ def kernel_source_hash(sources=None):
 
 
 def recorded_traffic(kv, workload=HEADLINE):
-    """DRAM bytes per paged_decode_attn call from a committed ncu summary, if it
-    was taken on the current kernel source and on this workload (the figures
-    are for the headline batch; else None)."""
-    if workload != HEADLINE:
-        return None
+    """DRAM bytes per paged_decode_attn call on ``workload`` from the committed
+    ncu summary (keys ``<workload>.<kv>.dram_bytes_per_call``), if it was taken
+    on the current kernel source; else None."""
     try:
         vals = {}
         with open(TRAFFIC_FILE) as f:
@@ -142,8 +144,9 @@ def recorded_traffic(kv, workload=HEADLINE):
                 if line and not line.startswith("#") and "=" in line:
                     k, v = line.split("=", 1)
                     vals[k.strip()] = v.strip()
-        if vals.get(kv + ".source_hash") == kernel_source_hash():
-            return {"dram_bytes_per_call": int(vals[kv + ".dram_bytes_per_call"])}
+        key = "%s.%s" % (workload, kv)
+        if vals.get(key + ".source_hash") == kernel_source_hash():
+            return {"dram_bytes_per_call": int(vals[key + ".dram_bytes_per_call"])}
     except Exception:
         pass
     return None
@@ -252,6 +255,17 @@ class Step:
     def check(self):
         self.fkv.kv_page_tag_check(self.page_tags, self.indptr, self.indices, self.expected, self.mask)
 
+    def append_check(self, separate=False):
+        """The step's append and integrity check: one launch for an FP8 cache
+        (kv_append_fp8_tag_check), or the two calls one after the other."""
+        if self.fp8 and not separate:
+            self.fkv.kv_append_fp8_tag_check(self.k_new, self.v_new, self.slots_new, self.k_scale, self.v_scale,
+                                             self.k_cache, self.v_cache, self.page_tags, self.indptr, self.indices,
+                                             self.expected, self.mask)
+        else:
+            self.append()
+            self.check()
+
     def attend(self, with_mask=True):
         self.fkv.paged_decode_attn(self.q, self.k_cache, self.v_cache, self.indptr, self.indices, self.seq_lens,
                                    self.sm, self.out, self.ws, k_scale=self.k_scale if self.fp8 else None,
@@ -259,7 +273,8 @@ class Step:
                                    abort_mask=self.mask if with_mask else None)
 
     def launches_per_step(self, with_check=True):
-        return (1 + (1 if with_check else 0) + self.fkv.kernels_per_call("paged_decode_attn"))
+        prologue = 1 if (self.fp8 or not with_check) else 2          # append (+ check)
+        return prologue + self.fkv.kernels_per_call("paged_decode_attn")
 
     def attn_bytes(self):
         """Algorithmic bytes of one paged_decode_attn call on the live requests:
@@ -278,9 +293,7 @@ class Step:
         torch = self.torch
         stream = torch.cuda.current_stream(self.device)
         for _ in range(warmup):
-            self.append()
-            if with_check:
-                self.check()
+            self.append_check() if with_check else self.append()
             self.attend(with_check)
         torch.cuda.synchronize(self.device)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
@@ -291,9 +304,7 @@ class Step:
         with ctx:
             t0.record(stream)
             for i in range(steps):
-                self.append()
-                if with_check:
-                    self.check()
+                self.append_check() if with_check else self.append()
                 ev[i][0].record(stream)
                 self.attend(with_check)
                 ev[i][1].record(stream)
@@ -304,17 +315,20 @@ class Step:
         attn_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
         return total_ms, attn_ms
 
-    def graph(self, with_check=True, checks_only=0, attn_only=False):
+    def graph(self, with_check=True, checks_only=0, attn_only=False, separate=False):
         """One step (or ``checks_only`` back-to-back checks, or the attention
         call alone) captured in a CUDA graph, so host launch cost is out of
-        the measurement."""
+        the measurement.  ``separate``: the check as its own launch after the
+        append instead of inside the append's launch."""
         torch = self.torch
         if attn_only:
             body = lambda: self.attend(True)
         elif checks_only:
             body = lambda: [self.check() for _ in range(checks_only)]
+        elif with_check:
+            body = lambda: (self.append_check(separate), self.attend(True))
         else:
-            body = lambda: (self.append(), self.check() if with_check else None, self.attend(with_check))
+            body = lambda: (self.append(), self.attend(False))
         body()                                    # one-time set-up happens outside the capture
         torch.cuda.synchronize(self.device)
         s = torch.cuda.Stream(self.device)
@@ -324,6 +338,20 @@ class Step:
             body()
         torch.cuda.synchronize(self.device)
         return g
+
+    def replay_ms(self, g, steps, warmup):
+        """Device time of ``steps`` back-to-back replays of a captured graph."""
+        torch = self.torch
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize(self.device)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(steps):
+            g.replay()
+        t1.record()
+        torch.cuda.synchronize(self.device)
+        return t0.elapsed_time(t1)
 
     def timed_graph(self, steps, warmup, with_check=True, checks_only=0, attn_only=False):
         torch = self.torch
@@ -341,13 +369,14 @@ class Step:
         barrier()
         return t0.elapsed_time(t1)
 
-    def timed_cold(self, reps, warmup):
-        """Median time of one captured step (append + check + attention) with
-        L2 flushed before each: a read of twice the L2 size between steps, so
-        the step reads its KV, page table and queries from HBM (a read, not a
-        write, leaves no dirty lines for the step to write back)."""
+    def timed_cold(self, reps, warmup, attn_only=False):
+        """Median time of one captured step (append + check + attention, or
+        the attention call alone) with L2 flushed before each: a read of twice
+        the L2 size between steps, so the step reads its KV, page table and
+        queries from HBM (a read, not a write, leaves no dirty lines for the
+        step to write back)."""
         torch = self.torch
-        g = self.graph(True, 0, False)
+        g = self.graph(True, 0, attn_only)
         l2 = int(getattr(torch.cuda.get_device_properties(self.device), "L2_cache_size", 0)) or (128 << 20)
         flush = torch.ones(2 * l2 // 4, dtype=torch.int32, device=self.device)
         sink = torch.empty((), dtype=torch.int32, device=self.device)
@@ -470,10 +499,11 @@ class Step:
             out, mask = ov[b]
             comp.wait_event(h2d[b])
             if self.fp8:
-                fkv.kv_append_fp8(kn, vn, sl, self.k_scale, self.v_scale, self.k_cache, self.v_cache)
+                fkv.kv_append_fp8_tag_check(kn, vn, sl, self.k_scale, self.v_scale, self.k_cache, self.v_cache,
+                                            tags, indptr, ind, exp, mask)
             else:
                 fkv.kv_append_bf16(kn, vn, sl, self.k_cache, self.v_cache)
-            fkv.kv_page_tag_check(tags, indptr, ind, exp, mask)
+                fkv.kv_page_tag_check(tags, indptr, ind, exp, mask)
             fkv.paged_decode_attn(q, self.k_cache, self.v_cache, indptr, ind, seq, self.sm, out, self.ws,
                                   k_scale=self.k_scale if self.fp8 else None,
                                   v_scale=self.v_scale if self.fp8 else None, abort_mask=mask)
@@ -610,13 +640,15 @@ def workload_text(wl, db):
 
 
 def run_reference(args):
-    """Reference arm: the CPU oracle as it stands.  Each step is one query-head
-    row of one request (its new token appended, its pages checked, that row
-    attended), cycling over all heads of the first few requests; the
-    requests' cached context is encoded by the oracle before timing."""
+    """Reference arm: the CPU oracle as it stands.  Each step is one request's
+    decode step -- its new token appended, its pages checked, all its query
+    heads attended, the rows split over the host's threads -- cycling over the
+    first few requests of the workload; their cached context is encoded by
+    the oracle before timing."""
     world, rank, local = dist_env()
     if rank != 0:
         return
+    import concurrent.futures as cf
     import torch
     import oracle
     from fp8_paged_kv_decode_gb300 import workloads as W
@@ -636,34 +668,135 @@ def run_reference(args):
     tags = db.pt.page_tags[cr.orig_pages]
     exp = np.concatenate([db.pt.expected_tags[db.pt.indptr[r]:db.pt.indptr[r + 1]] for r in range(n_req)])
     sm = 1.0 / np.sqrt(D)
+    threads = max(1, os.cpu_count() or 1)
     total = 0.0
-    for i in range(args.warmup + args.steps):
-        j = (i // Hq) % n_req
-        row = j * Hq + i % Hq
-        t0 = time.perf_counter()
-        orc.kv_append_fp8(cr.k_tokens[new_idx[j]:new_idx[j] + 1], cr.v_tokens[new_idx[j]:new_idx[j] + 1],
-                          cr.slots[new_idx[j]:new_idx[j] + 1], db.k_scale, db.v_scale, kc, vc)
-        mask = orc.kv_page_tag_check(tags, cr.indptr, cr.indices, exp)
-        orc.paged_decode_attn(cr.q, kc, vc, cr.indptr, cr.indices, cr.seq_lens, sm, k_scale=db.k_scale,
-                              v_scale=db.v_scale, abort_mask=mask, rows=[row])
-        if i >= args.warmup:
-            total += time.perf_counter() - t0
-    value = (args.steps / Hq) / total          # decode tokens/s: Hq rows make one request's token
-    sample = ("one query-head row per step (cycling over the %d heads of the first %d requests, %d context "
-              "tokens), with that request's append and tag check; 1 thread" % (Hq, n_req, int(cr.seq_lens.sum())))
+    with cf.ThreadPoolExecutor(threads) as ex:
+        for i in range(args.warmup + args.steps):
+            j = i % n_req
+            parts = [p for p in np.array_split(np.arange(j * Hq, (j + 1) * Hq, dtype=np.int32), threads) if p.size]
+            t0 = time.perf_counter()
+            orc.kv_append_fp8(cr.k_tokens[new_idx[j]:new_idx[j] + 1], cr.v_tokens[new_idx[j]:new_idx[j] + 1],
+                              cr.slots[new_idx[j]:new_idx[j] + 1], db.k_scale, db.v_scale, kc, vc)
+            mask = orc.kv_page_tag_check(tags, cr.indptr, cr.indices, exp)
+            list(ex.map(lambda rows: orc.paged_decode_attn(cr.q, kc, vc, cr.indptr, cr.indices, cr.seq_lens, sm,
+                                                           k_scale=db.k_scale, v_scale=db.v_scale,
+                                                           abort_mask=mask, rows=rows), parts))
+            if i >= args.warmup:
+                total += time.perf_counter() - t0
+    value = args.steps / total                 # decode tokens/s: one request's token per step
+    sample = ("one request's decode step per step (append, tag check, all %d query heads), cycling over the "
+              "first %d requests (%d context tokens); attention rows over %d host threads"
+              % (Hq, n_req, int(cr.seq_lens.sum()), threads))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_text(wl, db), "kv_dtype": "fp8_e4m3",
-                   "step": "CPU oracle: append + tag check + attention, one query-head row"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+                   "step": "CPU oracle: append + tag check + attention of one request"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def capacity_sweep(args):
+# The attention call on every workload: FP8 on all five, BF16 where the
+# workload compares the two, and the integrity workload both as specified
+# (1% of pages stale, most requests aborted) and with no stale page.
+CONFIG_LEGS = [("tiny_gqa4", "fp8", None), ("uniform_gqa8_8k", "fp8", None), ("uniform_gqa8_8k", "bf16", None),
+               ("pages_shaped_64req", "fp8", None), ("pages_shaped_64req", "bf16", None),
+               ("long_ctx_131k", "fp8", None), ("integrity_256req", "fp8", None), ("integrity_256req", "fp8", 0.0)]
+
+
+def l2_bytes(torch, device):
+    return int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0)) or (128 << 20)
+
+
+def config_table(device, rank, reps, warmup, peak, reuse=None):
+    """paged_decode_attn on each entry of CONFIG_LEGS: the call's device time
+    (CUDA-graph replays of the call alone), its algorithmic bytes on the live
+    requests, GB/s and the fraction of the measured copy peak, plus the DRAM
+    traffic of one launch from the committed ncu record when it matches the
+    current kernel.  Working sets below twice the L2 size are timed with L2
+    flushed before every call (a read of twice its size); larger ones stream
+    from HBM on every call anyway and are timed back to back."""
+    import dataclasses
+    import torch
+    from fp8_paged_kv_decode_gb300 import workloads as W
+    l2 = l2_bytes(torch, device)
+    out = {}
+    for name, kv, stale in CONFIG_LEGS:
+        wl = W.WORKLOADS[name]
+        key = name if stale is None else "%s_stale%g" % (name, stale)
+        if stale is not None:
+            wl = dataclasses.replace(wl, name=key, stale_frac=stale)
+        db = reuse if (reuse is not None and stale is None and reuse.wl.name == name) else \
+            W.device_batch(wl, device, seed=wl.seed + rank)
+        st = Step(db, kv, device)
+        st.check()                                   # the abort mask the timed calls read
+        torch.cuda.synchronize(device)
+        nbytes, attended = st.attn_bytes()
+        live = int(wl.batch - int(st.mask.sum().item()))
+        warm_us = 1e3 * max_over_ranks(st.timed_graph(reps, warmup, attn_only=True)) / reps
+        cold_us = 1e3 * max_over_ranks(st.timed_cold(reps, warmup, attn_only=True))
+        flushed = nbytes < 2 * l2
+        us = cold_us if flushed else warm_us
+        gbs = nbytes / (us * 1e3)
+        tr = recorded_traffic(kv, key)
+        out["%s.%s" % (key, kv)] = {
+            "workload": workload_text(wl, db), "kv": kv, "live_requests": live,
+            "attn_us": us, "attn_us_back_to_back": warm_us, "attn_us_l2_flushed": cold_us,
+            "timing": "L2 flushed before each call" if flushed else "back to back (working set > 2x L2)",
+            "algorithmic_bytes": nbytes, "gbs": gbs, "frac": gbs / peak, "frac_of_8tbs": gbs / 8000.0,
+            "tokens_per_s": live / (us * 1e-6), "context_tokens_per_s": attended / (us * 1e-6),
+            "traffic": tr["dram_bytes_per_call"] if tr else None,
+            "traffic_ratio": tr["dram_bytes_per_call"] / nbytes if tr else None}
+        del st
+        if db is not reuse:
+            del db
+        torch.cuda.empty_cache()
+    return out
+
+
+def bootstrap_ci(x, stat, n=10000, seed=0):
+    """95% percentile-bootstrap interval of ``stat`` over the samples ``x``."""
+    rng = np.random.default_rng(seed)
+    x = np.asarray(x, np.float64)
+    b = np.array([stat(x[rng.integers(0, x.size, x.size)]) for _ in range(n)])
+    return [float(np.percentile(b, 2.5)), float(np.percentile(b, 97.5))]
+
+
+def integrity_overhead(st, pairs, steps, warmup):
+    """Cost of the tag check in the decode step.  Three CUDA-graph-captured
+    steps -- without the check, with the check in the append's launch (the
+    step as run), with the check as a launch of its own -- are timed in
+    ``pairs`` interleaved rounds (the order rotates between rounds), ``steps``
+    replays each; per round the overhead of each variant is (with - without)
+    / without.  Returns the per-round figures, their median and mean and 95%
+    bootstrap intervals of both."""
+    graphs = {"off": st.graph(False), "on": st.graph(True), "separate": st.graph(True, separate=True)}
+    for g in graphs.values():
+        st.replay_ms(g, 0, warmup)
+    times = {k: [] for k in graphs}
+    order = list(graphs)
+    for i in range(pairs):
+        for k in order[i % 3:] + order[:i % 3]:
+            times[k].append(max_over_ranks(st.replay_ms(graphs[k], steps, 2)) / steps)
+    t = {k: np.array(v) for k, v in times.items()}
+    res = {"rounds": pairs, "steps_per_timing": steps,
+           "step_ms_without_check_median": float(np.median(t["off"])),
+           "step_ms_with_check_median": float(np.median(t["on"])),
+           "step_ms_with_separate_check_median": float(np.median(t["separate"]))}
+    for k, name in (("on", ""), ("separate", "separate_launch_")):
+        pct = 100.0 * (t[k] - t["off"]) / t["off"]
+        res.update({name + "overhead_pct_per_round": [float(v) for v in pct],
+                    name + "overhead_pct_median": float(np.median(pct)),
+                    name + "overhead_pct_median_ci95": bootstrap_ci(pct, np.median),
+                    name + "overhead_pct_mean": float(pct.mean()),
+                    name + "overhead_pct_mean_ci95": bootstrap_ci(pct, np.mean)})
+    return res
+
+
+def capacity_rows(db, device, steps, warmup):
     """A per-layer KV budget that holds the first 32 requests of the 64-request
     workload in BF16; how many requests each KV dtype admits under it, and the
     decode step (append + check + attention) at concurrency 1..64 for both,
@@ -672,20 +805,14 @@ def capacity_sweep(args):
     over the same pages keep a small batch's KV in L2, so each row also gives
     the step time with L2 flushed before every step."""
     import torch
-    import fp8_paged_kv_decode_gb300 as fkv
     from fp8_paged_kv_decode_gb300 import workloads as W
-    device = torch.device("cuda", 0)
-    torch.cuda.set_device(device)
-    fkv.load_library()
-    wl = W.WORKLOADS[HEADLINE]
-    db = W.device_batch(wl, device)
+    wl = db.wl
     npages = np.diff(db.pt.indptr)
     page_fp8 = 2 * wl.num_kv_heads * wl.page_size * wl.head_dim
     page_bf16 = 2 * page_fp8
     budget = int(npages[:32].sum()) * page_bf16
     adm = {"fp8": W.admitted(page_fp8, npages, budget), "bf16": W.admitted(page_bf16, npages, budget)}
     rows = []
-    steps = max(50, args.steps // 10)
     for c in sorted({1, 2, 4, 8, 16, 32, 48, 64, adm["fp8"], adm["bf16"]} - {0}):
         row = {"requests": c, "tokens": int(db.seq_lens[:c].sum())}
         sub = W.subset_batch(db, c)
@@ -694,21 +821,44 @@ def capacity_sweep(args):
                 row[kv] = None                      # does not fit the budget
                 continue
             st = Step(sub, kv, device)
-            tot = st.timed_graph(steps, args.warmup)                 # whole step, CUDA graph
-            attn = st.timed_graph(steps, args.warmup, attn_only=True)
-            cold = st.timed_cold(max(20, steps // 5), args.warmup)    # L2 flushed before each step
+            tot = st.timed_graph(steps, warmup)                      # whole step, CUDA graph
+            attn = st.timed_graph(steps, warmup, attn_only=True)
+            cold = st.timed_cold(max(20, steps // 5), warmup)         # L2 flushed before each step
             row[kv] = {"step_ms": tot / steps, "tokens_per_s": c / (tot / steps / 1e3), "attn_ms": attn / steps,
                        "step_ms_cold_l2": cold}
             del st
             torch.cuda.empty_cache()
         rows.append(row)
     peak = {kv: max((r[kv]["tokens_per_s"] for r in rows if r[kv]), default=0.0) for kv in ("fp8", "bf16")}
-    print(json.dumps({"capacity_sweep": {
-        "workload": workload_text(wl, db), "budget_bytes_per_layer": budget,
-        "budget": "BF16 pages of the first 32 requests", "admitted": adm,
-        "resident_tokens": {kv: int(db.seq_lens[:adm[kv]].sum()) for kv in adm},
-        "rows": rows, "peak_tokens_per_s": peak, "fp8_peak_over_bf16_peak": peak["fp8"] / peak["bf16"]}}),
-        flush=True)
+    return {"workload": workload_text(wl, db), "budget_bytes_per_layer": budget,
+            "budget": "BF16 pages of the first 32 requests", "admitted": adm,
+            "resident_tokens": {kv: int(db.seq_lens[:adm[kv]].sum()) for kv in adm},
+            "steps_per_timing": steps, "rows": rows, "peak_tokens_per_s": peak,
+            "fp8_peak_over_bf16_peak": peak["fp8"] / peak["bf16"]}
+
+
+def capacity_sweep(args):
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    from fp8_paged_kv_decode_gb300 import workloads as W
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    fkv.load_library()
+    db = W.device_batch(W.WORKLOADS[HEADLINE], device)
+    print(json.dumps({"capacity_sweep": capacity_rows(db, device, max(50, args.steps // 10), args.warmup)}),
+          flush=True)
+
+
+def configs_only(args):
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    fkv.load_library()
+    reps = args.config_reps or max(10, min(200, args.steps))
+    peak, kind = peak_hbm()
+    print(json.dumps({"configs": config_table(device, 0, reps, args.warmup, peak), "peak_gbs": peak,
+                      "peak_kind": kind}), flush=True)
 
 
 def shared_prefix(args):
@@ -758,6 +908,9 @@ def main():
     if args.shared_prefix:
         shared_prefix(args)
         return
+    if args.configs_only:
+        configs_only(args)
+        return
     world, rank, local = dist_env()
     import torch
     if world > 1:
@@ -789,8 +942,8 @@ def main():
     achieved = attn_bytes / (attn_ms / 1e3) / 1e9
     traffic = recorded_traffic(args.kv, wl.name)
 
-    e2e_steps = max(10, args.steps // 4)
-    e2e_ms, bi, bo = fp8.timed_e2e(e2e_steps, max(3, args.warmup // 4))
+    e2e_steps = args.steps
+    e2e_ms, bi, bo = fp8.timed_e2e(e2e_steps, max(3, args.warmup))
     e2e_ms = max_over_ranks(e2e_ms)
     e2e_value = world * wl.batch * e2e_steps / (e2e_ms / 1e3)
 
@@ -801,7 +954,8 @@ def main():
         "bf16 KV -> bf16 MMA, f32 accumulate", "data": "synthetic",
         "config": {"workload": workload_text(wl, db), "kv_dtype": "fp8_e4m3" if args.kv == "fp8" else "bf16",
                    "global_batch": world * wl.batch,
-                   "step": "kv_append_%s + kv_page_tag_check + paged_decode_attn (one layer)" % args.kv,
+                   "step": ("kv_append_fp8_tag_check (append + integrity check, one launch)" if args.kv == "fp8" else
+                            "kv_append_bf16 + kv_page_tag_check") + " + paged_decode_attn (one layer)",
                    "l2": "inputs larger than L2 (%.2f GB of KV read per step); no flush" % (attn_bytes / 1e9),
                    "parallelism": "replicas x%d" % world},
         "roofline": {"bound": "hbm", "kernel": "paged_decode_attn (plan + split attention with fused merge)",
@@ -833,15 +987,15 @@ def main():
         torch.cuda.empty_cache()
 
         # integrity check cost: the 0%-stale variant of integrity_256req with
-        # and without the check, each step captured in a CUDA graph
+        # and without the check, each step captured in a CUDA graph; repeated
+        # interleaved pairs give the spread
         import dataclasses
         iw = W.WORKLOADS["integrity_256req"]
         iw0 = dataclasses.replace(iw, stale_frac=0.0)
         idb = W.device_batch(iw0, device, seed=iw.seed + rank)
         ist = Step(idb, "fp8", device)
-        n_i = max(50, args.steps // 2)
-        on_ms = max_over_ranks(ist.timed_graph(n_i, args.warmup, with_check=True))
-        off_ms = max_over_ranks(ist.timed_graph(n_i, args.warmup, with_check=False))
+        n_i = max(200, args.steps // 2)
+        pairs = integrity_overhead(ist, 10, n_i, args.warmup)
         reps = 20
         chk_ms = max_over_ranks(ist.timed_graph(n_i // 10 + 1, 3, checks_only=reps))
         chk_us = 1e3 * chk_ms / ((n_i // 10 + 1) * reps)
@@ -855,15 +1009,23 @@ def main():
         realloc = sst.time_realloc(frac=0.01, reps=max(20, n_i // 10))
         line["integrity_check"] = {
             "workload": workload_text(iw, sdb),
-            "overhead_variant": "same shape, 0%% stale pages (%d aborted)" % clean_aborts,
-            "step_ms_with_check": on_ms / n_i, "step_ms_without_check": off_ms / n_i,
-            "overhead_pct": 100.0 * (on_ms - off_ms) / off_ms, "check_kernel_us": chk_us,
-            "check_share_of_step_pct": 100.0 * chk_us / (1e3 * on_ms / n_i),
+            "overhead_variant": "same shape, 0%% stale pages (%d aborted); the check runs in the append's launch "
+                                "(kv_append_fp8_tag_check), separate_launch_* as its own launch" % clean_aborts,
+            "overhead_pct": pairs["overhead_pct_median"], **pairs,
+            "check_kernel_us": chk_us,
+            "check_share_of_step_pct": 100.0 * chk_us / (1e3 * pairs["step_ms_with_check_median"]),
             "stale_1pct": {"aborted_requests": int(sst.mask.sum().item()), "step_ms": st_ms / n_i},
             "device_realloc_1pct": realloc,
             "timing": "CUDA-graph-captured steps"}
         del sst, sdb
         torch.cuda.empty_cache()
+
+        # every workload's attention call, and the capacity / concurrency sweep
+        line["configs"] = config_table(device, rank, args.config_reps or max(20, min(200, args.steps)),
+                                       args.warmup, peak, reuse=db)
+        del fp8
+        torch.cuda.empty_cache()
+        line["capacity_sweep"] = capacity_rows(db, device, max(50, args.steps // 10), args.warmup)
 
     derr = fkv.device_error()
     if derr:
