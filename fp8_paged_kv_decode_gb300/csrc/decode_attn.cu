@@ -102,6 +102,12 @@ constexpr int kMinAlignedTiles = FKV_ALIGNED_MIN_TILES;
 #ifndef FKV_LOCAL_PLAN_MAX
 #define FKV_LOCAL_PLAN_MAX 128
 #endif
+// At the end of its range a warp holding the last unfinished part of a unit
+// merges from its registers (1) instead of publishing its part and merging
+// through the stage ring (0).
+#ifndef FKV_TRY_LAST
+#define FKV_TRY_LAST 1
+#endif
 constexpr int kLocalPlanMax = FKV_LOCAL_PLAN_MAX;
 static_assert(kLocalPlanMax <= 1024, "one 32-request chunk per lane");
 // Attention CTA: one warp that both issues copies and computes, or (kWS) a
@@ -1174,10 +1180,16 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             mx[j] = fmaxf(mx[j], __shfl_xor_sync(kFull, mx[j], 8));
             mx[j] = fmaxf(mx[j], __shfl_xor_sync(kFull, mx[j], 16));
         }
+        // Each logit is scaled with one rounded multiply, the same operation
+        // that forms the running maximum, so the largest logit gives exactly
+        // ex2(0) = 1 and every other one at most 1.  (A fused multiply-add
+        // against the rounded maximum would leave the product's rounding error,
+        // up to half an ulp of the logit: harmless for ordinary logits, but
+        // past ~2^33 in log2 units that error overflows ex2.)
         float alpha[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const float mnew = fmaxf(m[j], mx[j] * cfac[j]);
+            const float mnew = fmaxf(m[j], __fmul_rn(mx[j], cfac[j]));
             alpha[j] = ex2(m[j] - mnew);
             m[j] = mnew;
         }
@@ -1187,7 +1199,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                pr[mt][c] = ex2(fmaf(sacc[mt][c], cfac[c & 1], -m[c & 1]));
+                pr[mt][c] = ex2(__fmul_rn(sacc[mt][c], cfac[c & 1]) - m[c & 1]);
                 ls[c & 1] += pr[mt][c];
             }
         l[0] = l[0] * alpha[0] + ls[0];
@@ -1292,10 +1304,82 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
             }
             const bool whole = seg_start == 0 && C.tt == C.nt - 1;
             const int64_t u = static_cast<int64_t>(C.r) * Hkv + C.h;
+            // parts of a split unit that hold tiles (warps of its span with a
+            // non-empty range)
+            auto unit_parts = [&](const UnitGeom &gm) {
+                int n = gm.span;
+                if (maybe_empty) {
+                    n = 0;
+                    for (int64_t x = gm.wf; x < gm.wf + gm.span; ++x) n += warp_lo(x, T, nw) != warp_lo(x + 1, T, nw);
+                }
+                return n;
+            };
+            bool merged = false;
+#if FKV_TRY_LAST
+            if (!whole && i == n_tiles - 1 && (maybe_empty || cgm.span <= kChunk)) {
+                // The unit's other parts usually end early in their warps'
+                // ranges, so at this warp's range end they may all have
+                // arrived.  Then this warp is the last: it merges its registers
+                // with their partials, loaded straight from global memory
+                // (one round trip for a unit over two warps), and writes the
+                // row -- no partial of its own, no arrival.  Otherwise it
+                // publishes and arrives as below.
+                int known = 0;
+                if (lane == 0) known = ld_acquire_gpu(p.counters + u) == unit_parts(cgm) - 1;
+                merged = __shfl_sync(kFull, known, 0) != 0;
+                if (merged) {
+                    __syncwarp();                              // lane 0's acquire covers the warp's loads
+                    const int d0 = kFp8 ? 16 * g : 8 * g, d1 = kFp8 ? 16 * g + 8 : 64 + 8 * g;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int hd = 2 * t + j;
+                        if (hd >= G) continue;
+                        float v[16];
+#pragma unroll
+                        for (int a = 0; a < 8; ++a) {
+                            v[2 * a] = o[a][j];
+                            v[2 * a + 1] = o[a][2 + j];
+                        }
+                        float Mj = m[j], Lj = lt[j];
+                        bool bad = unit_bad;
+                        for (int64_t x = cgm.wf; x < cgm.wf + cgm.span; ++x) {
+                            if (x == w || (maybe_empty && warp_lo(x, T, nw) == warp_lo(x + 1, T, nw))) continue;
+                            const int64_t slot = u + x;
+                            const float4 *prow = reinterpret_cast<const float4 *>(p.part_o + (slot * G + hd) * kD);
+                            const float2 ml = __ldcg(p.part_ml + slot * p.GP + hd);
+                            const float4 q0 = __ldcg(prow + d0 / 4), q1 = __ldcg(prow + d0 / 4 + 1);
+                            const float4 q2 = __ldcg(prow + d1 / 4), q3 = __ldcg(prow + d1 / 4 + 1);
+                            const float qv[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
+                                                  q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
+                            bad |= ml.y < 0.f;
+                            const float Mn = fmaxf(Mj, ml.x);
+                            const float a = ex2(Mj - Mn), b = ex2(ml.x - Mn);
+                            Lj = Lj * a + ml.y * b;
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] = v[e] * a + qv[e] * b;
+                            Mj = Mn;
+                        }
+                        const float f = bad ? 0.f : cvsc / Lj;
+                        __nv_bfloat16 *orow = p.out + (static_cast<int64_t>(C.r) * p.Hq + C.h * G + hd) * kD;
+                        uint4 r0v, r1v;
+                        r0v.x = pack_bf16x2(v[0] * f, v[1] * f);
+                        r0v.y = pack_bf16x2(v[2] * f, v[3] * f);
+                        r0v.z = pack_bf16x2(v[4] * f, v[5] * f);
+                        r0v.w = pack_bf16x2(v[6] * f, v[7] * f);
+                        r1v.x = pack_bf16x2(v[8] * f, v[9] * f);
+                        r1v.y = pack_bf16x2(v[10] * f, v[11] * f);
+                        r1v.z = pack_bf16x2(v[12] * f, v[13] * f);
+                        r1v.w = pack_bf16x2(v[14] * f, v[15] * f);
+                        *reinterpret_cast<uint4 *>(orow + d0) = r0v;
+                        *reinterpret_cast<uint4 *>(orow + d1) = r1v;
+                    }
+                }
+            }
+#endif
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int hd = 2 * t + j;
-                if (hd >= G) continue;
+                if (hd >= G || merged) continue;
                 // this lane's 16 dims of head hd, in ascending order
                 float v[16];
 #pragma unroll
@@ -1329,7 +1413,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                     if (g == 0) __stcg(p.part_ml + slot * p.GP + hd, make_float2(m[j], unit_bad ? -1.f : lt[j]));
                 }
             }
-            if (!whole) {
+            if (!whole && !merged) {
                 // Merge without waiting: the last of the unit's warps to arrive
                 // merges.  Units split over more than kChunk warps merge in two
                 // levels (chunks of kChunk consecutive parts, then the chunks),
@@ -1341,12 +1425,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                 int stage = kNone;
                 __syncwarp();
                 if (maybe_empty || gm.span <= kChunk) {
-                    int nparts = gm.span;
-                    if (maybe_empty) {
-                        nparts = 0;
-                        for (int64_t x = gm.wf; x < gm.wf + gm.span; ++x)
-                            nparts += warp_lo(x, T, nw) != warp_lo(x + 1, T, nw);
-                    }
+                    const int nparts = unit_parts(gm);
                     int last = 0;
                     if (lane == 0) last = atomic_add_acq_rel_gpu(p.counters + u, 1) == nparts - 1;
                     stage = __shfl_sync(kFull, last, 0) ? kFinalDue : kNone;

@@ -287,6 +287,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                  ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
+// Load at GPU scope with acquire semantics: what other threads released
+// before the value it returns is visible to this thread afterwards (and to
+// its warp after a warp barrier).
+__device__ __forceinline__ int ld_acquire_gpu(const int *addr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
 // Atomic add at GPU scope with acquire-release semantics: the caller's earlier
 // writes (and those of threads that synchronised with it) are visible before
 // the add, and writes released by earlier adders are visible after it.

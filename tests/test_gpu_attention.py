@@ -76,6 +76,20 @@ def test_wide_dynamic_range_q(orc, G, zero_k):
     assert_close(bf16_out(case.gpu()), case.oracle(orc), "G=%d zero_k=%s" % (G, zero_k))
 
 
+@pytest.mark.parametrize("m", [1e9, 1e12])
+@pytest.mark.parametrize("G", [4, 8])
+def test_huge_logits_stay_finite(orc, G, m):
+    """Query channels x1e9 or x1e12 with K random there: logits reach ~1e10
+    in log2 units.  The softmax scales each logit with the same rounded
+    multiply that forms the running maximum, so the largest term is exactly
+    1 and nothing overflows; the outputs are finite and match the oracle."""
+    case = PagedCase(orc, 4, G * 2, 2, 64, [3000, 100, 17, 800], seed=60 + G)
+    wide_range_q(case, [m, m, m / 10], seed=70 + G)
+    got = bf16_out(case.gpu())
+    assert np.isfinite(got).all()
+    assert_close(got, case.oracle(orc), "G=%d m=%g" % (G, m))
+
+
 @pytest.mark.parametrize("S", [16, 64])
 def test_fail_closed_rows(orc, S):
     """Aborted, empty, over-long and bad-page requests give zero rows; the
