@@ -277,16 +277,9 @@ class Step:
         return prologue + self.fkv.kernels_per_call("paged_decode_attn")
 
     def attn_bytes(self):
-        """Algorithmic bytes of one paged_decode_attn call on the live requests:
-        K and V of every attended token, q and out, page ids and seq_lens."""
-        mask = self.mask.cpu().numpy()
-        live = mask == 0
-        seq = self.db.seq_lens.astype(np.int64)
-        es = 1 if self.fp8 else 2
-        kv = int((seq[live] * self.Hkv * self.D * 2 * es).sum())
-        pages = int(((seq[live] + self.S - 1) // self.S).sum())
-        qo = self.B * self.Hq * self.D * 2 * 2
-        return kv + qo + 4 * pages + 4 * self.B, int(seq[live].sum())
+        """Algorithmic bytes of one paged_decode_attn call on the live requests
+        (the abort mask of the last check)."""
+        return algorithmic_attn_bytes(self.db, self.kv, self.mask.cpu().numpy())
 
     def timed(self, steps, warmup, with_check=True, sampler=None):
         """Device time of ``steps`` steps and of the attention calls within them."""
@@ -633,6 +626,30 @@ def oracle_sample(db, kv, n_requests, start=0, threads=1):
 
 
 # ----------------------------------------------------------------------------
+def algorithmic_attn_bytes(db, kv, mask):
+    """Algorithmic bytes of one paged_decode_attn call on the live requests
+    (mask[r] == 0): K and V of every attended token, q and out, page ids and
+    seq_lens."""
+    wl = db.wl
+    live = np.asarray(mask) == 0
+    seq = db.seq_lens.astype(np.int64)
+    es = 1 if kv == "fp8" else 2
+    kvb = int((seq[live] * wl.num_kv_heads * wl.head_dim * 2 * es).sum())
+    pages = int(((seq[live] + wl.page_size - 1) // wl.page_size).sum())
+    qo = wl.batch * wl.num_q_heads * wl.head_dim * 2 * 2
+    return kvb + qo + 4 * pages + 4 * wl.batch, int(seq[live].sum())
+
+
+def arm_config(wl, db, kv, world, attn_bytes):
+    """The ``config`` of the JSON line, the same for both arms."""
+    return {"workload": workload_text(wl, db), "kv_dtype": "fp8_e4m3" if kv == "fp8" else "bf16",
+            "global_batch": world * wl.batch,
+            "step": ("kv_append_fp8_tag_check (append + integrity check, one launch)" if kv == "fp8" else
+                     "kv_append_bf16 + kv_page_tag_check") + " + paged_decode_attn (one layer)",
+            "l2": "inputs larger than L2 (%.2f GB of KV read per step); no flush" % (attn_bytes / 1e9),
+            "parallelism": "replicas x%d" % world}
+
+
 def workload_text(wl, db):
     return ("%s: %d req, %d q / %d kv heads, head_dim %d, page %d, ctx %s, %d tokens attended per step"
             % (wl.name, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.page_size, wl.ctx,
@@ -684,15 +701,18 @@ def run_reference(args):
             if i >= args.warmup:
                 total += time.perf_counter() - t0
     value = args.steps / total                 # decode tokens/s: one request's token per step
-    sample = ("one request's decode step per step (append, tag check, all %d query heads), cycling over the "
-              "first %d requests (%d context tokens); attention rows over %d host threads"
+    sample = ("CPU oracle, one request's decode step per step (append, tag check, all %d query heads), cycling "
+              "over the first %d requests (%d context tokens); attention rows over %d host threads"
               % (Hq, n_req, int(cr.seq_lens.sum()), threads))
+    # the same config as the GPU arm's line: its algorithmic bytes from the
+    # whole batch's abort mask, which the oracle computes here
+    full_mask = orc.kv_page_tag_check(db.pt.page_tags, db.pt.indptr, db.pt.indices, db.pt.expected_tags)
+    attn_bytes, _ = algorithmic_attn_bytes(db, "fp8", full_mask)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_text(wl, db), "kv_dtype": "fp8_e4m3",
-                   "step": "CPU oracle: append + tag check + attention of one request"},
+        "config": arm_config(wl, db, "fp8", world, attn_bytes),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -952,12 +972,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 KV -> f16 MMA, f32 accumulate" if args.kv == "fp8" else
         "bf16 KV -> bf16 MMA, f32 accumulate", "data": "synthetic",
-        "config": {"workload": workload_text(wl, db), "kv_dtype": "fp8_e4m3" if args.kv == "fp8" else "bf16",
-                   "global_batch": world * wl.batch,
-                   "step": ("kv_append_fp8_tag_check (append + integrity check, one launch)" if args.kv == "fp8" else
-                            "kv_append_bf16 + kv_page_tag_check") + " + paged_decode_attn (one layer)",
-                   "l2": "inputs larger than L2 (%.2f GB of KV read per step); no flush" % (attn_bytes / 1e9),
-                   "parallelism": "replicas x%d" % world},
+        "config": arm_config(wl, db, args.kv, world, attn_bytes),
         "roofline": {"bound": "hbm", "kernel": "paged_decode_attn (plan + split attention with fused merge)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "traffic": traffic["dram_bytes_per_call"] if traffic else None,
