@@ -6,8 +6,10 @@
  * over a pool with spare pages) is drawn from a fixed-seed generator.  On the
  * device: per-head scales of the context (kv_calibrate_scales), the whole
  * context written as e4m3 (kv_append_fp8), the integrity check with one stale
- * tag (kv_page_tag_check), then attention (paged_decode_attn).  The scales,
- * every pool byte and the abort mask must equal the oracle's bit for bit; the
+ * tag (kv_page_tag_check), then attention (paged_decode_attn); and the same
+ * append and check once more as one launch (kv_append_fp8_tag_check) into a
+ * second pair of pools.  The scales, every pool byte of both pairs and both
+ * abort masks must equal the oracle's bit for bit; the
  * attention rows must be within the tolerance (an element fails only if it is
  * off by more than 2e-3 absolute and 1e-2 relative), the aborted row zero. */
 #include <math.h>
@@ -165,6 +167,15 @@ int main(void) {
     FK(kv_calibrate_scales(dk, dv, ntok, HKV, D, dks, dvs, NULL));
     FK(kv_append_fp8(dk, dv, dslots, ntok, dks, dvs, dkc, dvc, P, HKV, S, D, NULL));
     FK(kv_page_tag_check(dtags, P, dindptr, dindices, dexp, B, nnz, dmask, NULL));
+    /* the same append and check in one launch, into a second pair of pools and a second mask */
+    uint8_t *dkc2, *dvc2, *dmask2;
+    CK(cudaMalloc((void **)&dkc2, pool));
+    CK(cudaMalloc((void **)&dvc2, pool));
+    CK(cudaMalloc((void **)&dmask2, B));
+    CK(cudaMemset(dkc2, 0, pool));
+    CK(cudaMemset(dvc2, 0, pool));
+    FK(kv_append_fp8_tag_check(dk, dv, dslots, ntok, dks, dvs, dkc2, dvc2, P, HKV, S, D, dtags, dindptr, dindices,
+                               dexp, B, nnz, dmask2, NULL));
     FK(paged_decode_attn(dq, B, HQ, dkc, dvc, FKV_KV_FP8_E4M3, dks, dvs, P, HKV, S, D, dindptr, dindices, nnz,
                          dseq, dmask, sm_scale, dout, dws, ws_bytes, NULL));
     CK(cudaDeviceSynchronize());
@@ -179,6 +190,10 @@ int main(void) {
     CK(cudaMemcpy(gkc, dkc, pool, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(gvc, dvc, pool, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(gmask, dmask, B, cudaMemcpyDeviceToHost));
+    uint8_t *gkc2 = malloc(pool), *gvc2 = malloc(pool), gmask2[B];
+    CK(cudaMemcpy(gkc2, dkc2, pool, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(gvc2, dvc2, pool, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(gmask2, dmask2, B, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(gout, dout, 2u * B * HQ * D, cudaMemcpyDeviceToHost));
 
     /* the oracle */
@@ -198,6 +213,10 @@ int main(void) {
     }
     if (memcmp(gkc, okc, pool) || memcmp(gvc, ovc, pool)) {
         fprintf(stderr, "pool bytes differ from the oracle\n");
+        ++fails;
+    }
+    if (memcmp(gkc2, okc, pool) || memcmp(gvc2, ovc, pool) || memcmp(gmask2, omask, B)) {
+        fprintf(stderr, "the append-and-check launch differs from the oracle\n");
         ++fails;
     }
     if (memcmp(gmask, omask, B) || omask[1] != 1 || omask[0] != 0 || omask[2] != 0) {

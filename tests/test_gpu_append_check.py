@@ -113,3 +113,24 @@ def test_integrity_workload_step(orc):
     vc = np.zeros_like(kc)
     orc.kv_append_fp8(kb, vb, slots, ks, vs, kc, vc)
     assert np.array_equal(kt.cpu().numpy(), kc) and np.array_equal(vt.cpu().numpy(), vc)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fuzz_combined(orc, seed):
+    """Random pool sizes, head counts, page sizes, token and request counts
+    and injected faults: the one-launch call matches the oracle and the two
+    separate calls bit for bit.  (Zero tokens or zero requests:
+    test_check_only_and_append_only.)"""
+    rng = np.random.default_rng(900 + seed)
+    S = int(rng.choice([16, 32, 64, 128]))
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    P = int(rng.integers(4, 400))
+    N = int(rng.integers(0, min(P * S, 600) + 1))
+    B = int(rng.integers(0, 300))
+    if N == 0 and B == 0:
+        B = 1
+    gk, gv, gm, kc, vc, want = _run(orc, P, Hkv, S, N, B, seed=1000 + seed, combined=True, faults=bool(seed % 3))
+    assert np.array_equal(gk, kc) and np.array_equal(gv, vc), "pool bytes differ from the oracle"
+    assert np.array_equal(gm, want), "abort mask differs from the oracle"
+    sk, sv, sm, _, _, _ = _run(orc, P, Hkv, S, N, B, seed=1000 + seed, combined=False, faults=bool(seed % 3))
+    assert np.array_equal(gk, sk) and np.array_equal(gv, sv) and np.array_equal(gm, sm)
