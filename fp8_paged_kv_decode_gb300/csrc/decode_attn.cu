@@ -1314,6 +1314,74 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                 }
                 return n;
             };
+            // The unit's final merge from this warp's registers plus the other
+            // parts' partials, loaded straight from L2 (one round trip per
+            // part), written as the bf16 row.  The caller has acquired every
+            // other part.
+            auto merge_regs = [&](int64_t u) {
+                const int d0 = kFp8 ? 16 * g : 8 * g, d1 = kFp8 ? 16 * g + 8 : 64 + 8 * g;
+                float v[2][16], Mj[2], Lj[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                    for (int a = 0; a < 8; ++a) {
+                        v[j][2 * a] = o[a][j];
+                        v[j][2 * a + 1] = o[a][2 + j];
+                    }
+                    Mj[j] = m[j];
+                    Lj[j] = lt[j];
+                }
+                bool bad = unit_bad;
+                for (int64_t x = cgm.wf; x < cgm.wf + cgm.span; ++x) {
+                    if (x == w || (maybe_empty && warp_lo(x, T, nw) == warp_lo(x + 1, T, nw))) continue;
+                    const int64_t slot = u + x;
+                    // both heads' loads of this part go out together (one round trip);
+                    // lanes past the group's heads read a valid row and drop it
+                    float2 ml[2];
+                    float4 q[2][4];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int hd = min(2 * t + j, G - 1);
+                        const float4 *prow = reinterpret_cast<const float4 *>(p.part_o + (slot * G + hd) * kD);
+                        ml[j] = __ldcg(p.part_ml + slot * p.GP + hd);
+                        q[j][0] = __ldcg(prow + d0 / 4);
+                        q[j][1] = __ldcg(prow + d0 / 4 + 1);
+                        q[j][2] = __ldcg(prow + d1 / 4);
+                        q[j][3] = __ldcg(prow + d1 / 4 + 1);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const float qv[16] = {q[j][0].x, q[j][0].y, q[j][0].z, q[j][0].w, q[j][1].x, q[j][1].y,
+                                              q[j][1].z, q[j][1].w, q[j][2].x, q[j][2].y, q[j][2].z, q[j][2].w,
+                                              q[j][3].x, q[j][3].y, q[j][3].z, q[j][3].w};
+                        bad |= ml[j].y < 0.f;
+                        const float Mn = fmaxf(Mj[j], ml[j].x);
+                        const float a = ex2(Mj[j] - Mn), b = ex2(ml[j].x - Mn);
+                        Lj[j] = Lj[j] * a + ml[j].y * b;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[j][e] = v[j][e] * a + qv[e] * b;
+                        Mj[j] = Mn;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int hd = 2 * t + j;
+                    if (hd >= G) continue;
+                    const float f = bad ? 0.f : cvsc / Lj[j];
+                    __nv_bfloat16 *orow = p.out + (static_cast<int64_t>(C.r) * p.Hq + C.h * G + hd) * kD;
+                    uint4 r0v, r1v;
+                    r0v.x = pack_bf16x2(v[j][0] * f, v[j][1] * f);
+                    r0v.y = pack_bf16x2(v[j][2] * f, v[j][3] * f);
+                    r0v.z = pack_bf16x2(v[j][4] * f, v[j][5] * f);
+                    r0v.w = pack_bf16x2(v[j][6] * f, v[j][7] * f);
+                    r1v.x = pack_bf16x2(v[j][8] * f, v[j][9] * f);
+                    r1v.y = pack_bf16x2(v[j][10] * f, v[j][11] * f);
+                    r1v.z = pack_bf16x2(v[j][12] * f, v[j][13] * f);
+                    r1v.w = pack_bf16x2(v[j][14] * f, v[j][15] * f);
+                    *reinterpret_cast<uint4 *>(orow + d0) = r0v;
+                    *reinterpret_cast<uint4 *>(orow + d1) = r1v;
+                }
+            };
             bool merged = false;
 #if FKV_TRY_LAST
             if (!whole && i == n_tiles - 1 && (maybe_empty || cgm.span <= kChunk)) {
@@ -1329,50 +1397,7 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                 merged = __shfl_sync(kFull, known, 0) != 0;
                 if (merged) {
                     __syncwarp();                              // lane 0's acquire covers the warp's loads
-                    const int d0 = kFp8 ? 16 * g : 8 * g, d1 = kFp8 ? 16 * g + 8 : 64 + 8 * g;
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const int hd = 2 * t + j;
-                        if (hd >= G) continue;
-                        float v[16];
-#pragma unroll
-                        for (int a = 0; a < 8; ++a) {
-                            v[2 * a] = o[a][j];
-                            v[2 * a + 1] = o[a][2 + j];
-                        }
-                        float Mj = m[j], Lj = lt[j];
-                        bool bad = unit_bad;
-                        for (int64_t x = cgm.wf; x < cgm.wf + cgm.span; ++x) {
-                            if (x == w || (maybe_empty && warp_lo(x, T, nw) == warp_lo(x + 1, T, nw))) continue;
-                            const int64_t slot = u + x;
-                            const float4 *prow = reinterpret_cast<const float4 *>(p.part_o + (slot * G + hd) * kD);
-                            const float2 ml = __ldcg(p.part_ml + slot * p.GP + hd);
-                            const float4 q0 = __ldcg(prow + d0 / 4), q1 = __ldcg(prow + d0 / 4 + 1);
-                            const float4 q2 = __ldcg(prow + d1 / 4), q3 = __ldcg(prow + d1 / 4 + 1);
-                            const float qv[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
-                                                  q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
-                            bad |= ml.y < 0.f;
-                            const float Mn = fmaxf(Mj, ml.x);
-                            const float a = ex2(Mj - Mn), b = ex2(ml.x - Mn);
-                            Lj = Lj * a + ml.y * b;
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) v[e] = v[e] * a + qv[e] * b;
-                            Mj = Mn;
-                        }
-                        const float f = bad ? 0.f : cvsc / Lj;
-                        __nv_bfloat16 *orow = p.out + (static_cast<int64_t>(C.r) * p.Hq + C.h * G + hd) * kD;
-                        uint4 r0v, r1v;
-                        r0v.x = pack_bf16x2(v[0] * f, v[1] * f);
-                        r0v.y = pack_bf16x2(v[2] * f, v[3] * f);
-                        r0v.z = pack_bf16x2(v[4] * f, v[5] * f);
-                        r0v.w = pack_bf16x2(v[6] * f, v[7] * f);
-                        r1v.x = pack_bf16x2(v[8] * f, v[9] * f);
-                        r1v.y = pack_bf16x2(v[10] * f, v[11] * f);
-                        r1v.z = pack_bf16x2(v[12] * f, v[13] * f);
-                        r1v.w = pack_bf16x2(v[14] * f, v[15] * f);
-                        *reinterpret_cast<uint4 *>(orow + d0) = r0v;
-                        *reinterpret_cast<uint4 *>(orow + d1) = r1v;
-                    }
+                    merge_regs(u);
                 }
             }
 #endif

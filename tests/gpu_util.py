@@ -1,6 +1,10 @@
 """Helpers shared by the GPU parity tests (argument plumbing only)."""
 from __future__ import annotations
 
+import os
+import shutil
+import subprocess
+
 import numpy as np
 
 from fp8_paged_kv_decode_gb300 import workloads as W
@@ -101,3 +105,33 @@ class PagedCase:
                               k_scale=ks, v_scale=vs, abort_mask=am)
         torch.cuda.synchronize()
         return out
+
+
+TESTS_DIR = os.path.dirname(os.path.abspath(__file__))
+REPO_ROOT = os.path.dirname(TESTS_DIR)
+
+
+def cuda_home():
+    for cand in (os.environ.get("CUDA_HOME"), "/usr/local/cuda"):
+        if cand and os.path.isdir(os.path.join(cand, "include")):
+            return cand
+    nvcc = shutil.which("nvcc")
+    return os.path.dirname(os.path.dirname(nvcc)) if nvcc else None
+
+
+def build_c_program(source, exe):
+    """Compile a plain C test program in tests/ against libfkv.so, the CUDA
+    runtime and the C oracle (gcc, no fast-math); returns the executable."""
+    import fp8_paged_kv_decode_gb300 as fkv
+    lib = fkv.library_path()
+    assert os.path.exists(lib), "libfkv.so is not built"
+    cuda = cuda_home()
+    assert cuda, "CUDA toolkit not found"
+    libdir = os.path.dirname(lib)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                    "-I", os.path.join(REPO_ROOT, "include"), "-I", os.path.join(cuda, "include"),
+                    os.path.join(TESTS_DIR, source), os.path.join(REPO_ROOT, "oracle", "fkv_oracle.c"),
+                    "-o", exe, "-L", libdir, "-l:" + os.path.basename(lib),
+                    "-L", os.path.join(cuda, "lib64"), "-lcudart", "-lm", "-Wl,-rpath," + libdir],
+                   check=True)
+    return exe

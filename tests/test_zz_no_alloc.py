@@ -14,13 +14,11 @@ by every attention test.  A plain C program then drives the entry point
 through the C ABI alone, across a cudaDeviceReset, and checks it against the
 C oracle.  The file is named so pytest collects it last.
 """
-import os
 import subprocess
 
-import numpy as np
 import pytest
 
-from gpu_util import PagedCase, assert_close, bf16_out, dev
+from gpu_util import PagedCase, assert_close, bf16_out, build_c_program, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -60,20 +58,7 @@ def test_noalloc_c_abi_across_device_reset(tmp_path):
     """Plain C, no torch: two calls in a row, then cudaDeviceReset (a new
     context, in which the library looks its scratch address up again), then a
     third call; all checked against the C oracle."""
-    import fp8_paged_kv_decode_gb300 as fkv
-    from test_gpu_c_abi import ROOT, HERE, _cuda_home
-    lib = fkv.library_path()
-    assert os.path.exists(lib), "libfkv.so is not built"
-    cuda = _cuda_home()
-    assert cuda, "CUDA toolkit not found"
-    libdir = os.path.dirname(lib)
-    exe = str(tmp_path / "c_abi_noalloc")
-    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
-                    "-I", os.path.join(ROOT, "include"), "-I", os.path.join(cuda, "include"),
-                    os.path.join(HERE, "c_abi_noalloc.c"), os.path.join(ROOT, "oracle", "fkv_oracle.c"),
-                    "-o", exe, "-L", libdir, "-l:" + os.path.basename(lib),
-                    "-L", os.path.join(cuda, "lib64"), "-lcudart", "-lm", "-Wl,-rpath," + libdir],
-                   check=True)
+    exe = build_c_program("c_abi_noalloc.c", str(tmp_path / "c_abi_noalloc"))
     res = subprocess.run([exe], capture_output=True, text=True, timeout=300)
     assert res.returncode == 0, res.stdout + res.stderr
     assert "c abi noalloc ok" in res.stdout, res.stdout
