@@ -308,20 +308,24 @@ class Step:
         attn_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
         return total_ms, attn_ms
 
-    def graph(self, with_check=True, checks_only=0, attn_only=False, separate=False):
+    def graph(self, with_check=True, checks_only=0, attn_only=False, separate=False, repeat=1):
         """One step (or ``checks_only`` back-to-back checks, or the attention
         call alone) captured in a CUDA graph, so host launch cost is out of
-        the measurement.  ``separate``: the check as its own launch after the
-        append instead of inside the append's launch."""
+        the measurement; ``repeat`` steps back to back in the one graph, as a
+        serving loop runs them (graph launches themselves are paced in ~2 us
+        steps, which would swamp a step of a few tens of us).  ``separate``:
+        the check as its own launch after the append instead of inside the
+        append's launch."""
         torch = self.torch
         if attn_only:
-            body = lambda: self.attend(True)
+            one = lambda: self.attend(True)
         elif checks_only:
-            body = lambda: [self.check() for _ in range(checks_only)]
+            one = lambda: [self.check() for _ in range(checks_only)]
         elif with_check:
-            body = lambda: (self.append_check(separate), self.attend(True))
+            one = lambda: (self.append_check(separate), self.attend(True))
         else:
-            body = lambda: (self.append(), self.attend(False))
+            one = lambda: (self.append(), self.attend(False))
+        body = lambda: [one() for _ in range(repeat)]
         body()                                    # one-time set-up happens outside the capture
         torch.cuda.synchronize(self.device)
         s = torch.cuda.Stream(self.device)
@@ -346,9 +350,11 @@ class Step:
         torch.cuda.synchronize(self.device)
         return t0.elapsed_time(t1)
 
-    def timed_graph(self, steps, warmup, with_check=True, checks_only=0, attn_only=False):
+    def timed_graph(self, steps, warmup, with_check=True, checks_only=0, attn_only=False, repeat=1):
+        """Device time of ``steps`` replays of the captured step (``repeat``
+        steps per replay: divide by steps * repeat for one step)."""
         torch = self.torch
-        g = self.graph(with_check, checks_only, attn_only)
+        g = self.graph(with_check, checks_only, attn_only, repeat=repeat)
         for _ in range(warmup):
             g.replay()
         torch.cuda.synchronize(self.device)
@@ -762,7 +768,14 @@ def config_table(device, rank, reps, warmup, peak, reuse=None):
         us = cold_us if flushed else warm_us
         gbs = nbytes / (us * 1e3)
         tr = recorded_traffic(kv, key)
-        out["%s.%s" % (key, kv)] = {
+        extra = {}
+        if name == "long_ctx_131k":
+            # spread of the logits q.k / sqrt(d) the workload is drawn for
+            # (std ~4): request 0, one query head per KV head, its first 4096 tokens
+            q = db.q[0, ::wl.group].float()
+            k = db.k_src[:4096].float()
+            extra["logit_std"] = float((torch.einsum("hd,thd->th", q, k) / np.sqrt(wl.head_dim)).std())
+        out["%s.%s" % (key, kv)] = {**extra,
             "workload": workload_text(wl, db), "kv": kv, "live_requests": live,
             "attn_us": us, "attn_us_back_to_back": warm_us, "attn_us_l2_flushed": cold_us,
             "timing": "L2 flushed before each call" if flushed else "back to back (working set > 2x L2)",
@@ -785,7 +798,7 @@ def bootstrap_ci(x, stat, n=10000, seed=0):
     return [float(np.percentile(b, 2.5)), float(np.percentile(b, 97.5))]
 
 
-def integrity_overhead(st, pairs, steps, warmup):
+def integrity_overhead(st, pairs, steps, warmup, repeat=1):
     """Cost of the tag check in the decode step.  Three CUDA-graph-captured
     steps -- without the check, with the check in the append's launch (the
     step as run), with the check as a launch of its own -- are timed in
@@ -793,16 +806,17 @@ def integrity_overhead(st, pairs, steps, warmup):
     replays each; per round the overhead of each variant is (with - without)
     / without.  Returns the per-round figures, their median and mean and 95%
     bootstrap intervals of both."""
-    graphs = {"off": st.graph(False), "on": st.graph(True), "separate": st.graph(True, separate=True)}
+    graphs = {"off": st.graph(False, repeat=repeat), "on": st.graph(True, repeat=repeat),
+              "separate": st.graph(True, separate=True, repeat=repeat)}
     for g in graphs.values():
         st.replay_ms(g, 0, warmup)
     times = {k: [] for k in graphs}
     order = list(graphs)
     for i in range(pairs):
         for k in order[i % 3:] + order[:i % 3]:
-            times[k].append(max_over_ranks(st.replay_ms(graphs[k], steps, 2)) / steps)
+            times[k].append(max_over_ranks(st.replay_ms(graphs[k], steps, 2)) / (steps * repeat))
     t = {k: np.array(v) for k, v in times.items()}
-    res = {"rounds": pairs, "steps_per_timing": steps,
+    res = {"rounds": pairs, "steps_per_timing": steps * repeat, "steps_per_graph": repeat,
            "step_ms_without_check_median": float(np.median(t["off"])),
            "step_ms_with_check_median": float(np.median(t["on"])),
            "step_ms_with_separate_check_median": float(np.median(t["separate"]))}
@@ -841,8 +855,10 @@ def capacity_rows(db, device, steps, warmup):
                 row[kv] = None                      # does not fit the budget
                 continue
             st = Step(sub, kv, device)
-            tot = st.timed_graph(steps, warmup)                      # whole step, CUDA graph
-            attn = st.timed_graph(steps, warmup, attn_only=True)
+            rep = 20 if c <= 16 else 1                              # short steps: many per graph
+            n = max(5, steps // rep)
+            tot = st.timed_graph(n, warmup, repeat=rep) * steps / (n * rep)   # whole step, CUDA graph
+            attn = st.timed_graph(n, warmup, attn_only=True, repeat=rep) * steps / (n * rep)
             cold = st.timed_cold(max(20, steps // 5), warmup)         # L2 flushed before each step
             row[kv] = {"step_ms": tot / steps, "tokens_per_s": c / (tot / steps / 1e3), "attn_ms": attn / steps,
                        "step_ms_cold_l2": cold}
@@ -1022,8 +1038,22 @@ def main():
         sst = Step(sdb, "fp8", device)
         st_ms = max_over_ranks(sst.timed_graph(n_i, args.warmup, with_check=True))
         realloc = sst.time_realloc(frac=0.01, reps=max(20, n_i // 10))
+        # the same rounds at concurrency 1, 2, 4 and 8 (the first N requests;
+        # the pages report the check's cost at these concurrencies)
+        cdb = W.device_batch(iw0, device, seed=iw.seed + rank)
+        by_conc = {}
+        for n in (1, 2, 4, 8):
+            cst = Step(W.subset_batch(cdb, n), "fp8", device)
+            r = integrity_overhead(cst, 10, max(10, n_i // 20), args.warmup, repeat=20)
+            by_conc[str(n)] = {k: r[k] for k in ("overhead_pct_median", "overhead_pct_median_ci95",
+                                                 "separate_launch_overhead_pct_median",
+                                                 "step_ms_without_check_median", "step_ms_with_check_median")}
+            del cst
+        del cdb
+        torch.cuda.empty_cache()
         line["integrity_check"] = {
             "workload": workload_text(iw, sdb),
+            "by_concurrency": by_conc,
             "overhead_variant": "same shape, 0%% stale pages (%d aborted); the check runs in the append's launch "
                                 "(kv_append_fp8_tag_check), separate_launch_* as its own launch" % clean_aborts,
             "overhead_pct": pairs["overhead_pct_median"], **pairs,

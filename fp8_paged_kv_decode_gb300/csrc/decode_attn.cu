@@ -77,7 +77,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;     // a copy that has not land
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr uint32_t kFull = 0xffffffffu;
 #ifndef FKV_MERGE_CHUNK
-#define FKV_MERGE_CHUNK 6
+#define FKV_MERGE_CHUNK 9
 #endif
 // Small batches may give each (request, KV head) unit whole warps (1) instead
 // of an even split of the batch's tiles (0); ranges then hold at least
@@ -107,6 +107,13 @@ constexpr int kMinAlignedTiles = FKV_ALIGNED_MIN_TILES;
 // through the stage ring (0).
 #ifndef FKV_TRY_LAST
 #define FKV_TRY_LAST 1
+#endif
+// A warp that becomes the last of a unit's parts in the middle of its range
+// (the tail of the unit it started in) records the merge and performs it at
+// its range end through the idle stage ring (1), instead of stalling its
+// stream for a merge through registers there (0).
+#ifndef FKV_DEFER_MIDRANGE
+#define FKV_DEFER_MIDRANGE 1
 #endif
 constexpr int kLocalPlanMax = FKV_LOCAL_PLAN_MAX;
 static_assert(kLocalPlanMax <= 1024, "one 32-request chunk per lane");
@@ -1016,6 +1023,13 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     bool unit_bad = false;
     float cvsc = 1.f;       // the unit's V scale
     UnitGeom cgm = agm;     // where the unit's parts sit, if it is split (span 0: not yet known)
+#if FKV_DEFER_MIDRANGE
+    // a merge this warp owes from the middle of its range: at most one, since
+    // only the unit it started in can end there and be split
+    int def_stage = kNone, def_r = 0, def_h = 0;
+    UnitGeom def_gm{0, 0};
+    float def_vsc = 1.f;
+#endif
 
     for (int64_t i = 0; i < n_tiles; ++i) {
         const int s = static_cast<int>(i % NST);
@@ -1464,11 +1478,28 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                     stage = __shfl_sync(kFull, last, 0) ? kChunkDue : kNone;
                 }
                 // at the range end the stage ring is idle: merge through it
+#if FKV_DEFER_MIDRANGE
+                if (stage != kNone && i < n_tiles - 1) {
+                    // mid-range: the stream would stall for the merge, and a
+                    // part ending just before this range's end can be the last
+                    // to arrive, putting that stall on the call's critical path;
+                    // owe it until the range end instead
+                    def_stage = stage;
+                    def_gm = gm;
+                    def_r = C.r;
+                    def_h = C.h;
+                    def_vsc = cvsc;
+                    stage = kNone;
+                }
+#endif
                 if (stage != kNone) merge_steps(stage, gm, C.r, C.h, cvsc, i == n_tiles - 1);
             }
         }
         cursor_next(C, p);
     }
+#if FKV_DEFER_MIDRANGE
+    if (def_stage != kNone) merge_steps(def_stage, def_gm, def_r, def_h, def_vsc, true);
+#endif
     grid_dep_launch();
 }
 
