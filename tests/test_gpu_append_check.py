@@ -134,3 +134,49 @@ def test_fuzz_combined(orc, seed):
     assert np.array_equal(gm, want), "abort mask differs from the oracle"
     sk, sv, sm, _, _, _ = _run(orc, P, Hkv, S, N, B, seed=1000 + seed, combined=False, faults=bool(seed % 3))
     assert np.array_equal(gk, sk) and np.array_equal(gv, sv) and np.array_equal(gm, sm)
+
+
+def test_small_integrity_step_after_one_launch_prologue(orc):
+    """The first 8 requests of the integrity workload (no stale page), step
+    after step: the append-and-check launch, then attention.  In this shape a
+    warp whose part of a unit ends one tile before its range end can be the
+    last of the unit's parts to arrive, and then owes the unit's merge in the
+    middle of its range (which it performs at its range end).  Every step's
+    rows must match the oracle on the cache as it stands after that step's
+    append."""
+    import dataclasses
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    from gpu_util import assert_close, bf16_out
+    wl = dataclasses.replace(W.WORKLOADS["integrity_256req"], stale_frac=0.0, batch=8)
+    hb = W.host_batch(wl)
+    P, Hkv, S, D = hb.pt.num_pages, wl.num_kv_heads, wl.page_size, wl.head_dim
+    kc = np.zeros((P, Hkv, S, D), np.uint8)
+    vc = np.zeros_like(kc)
+    orc.kv_append_fp8(hb.k_src, hb.v_src, hb.slots_src, hb.k_scale, hb.v_scale, kc, vc)
+    kt, vt = dev(kc), dev(vc)
+    ks, vs = dev(hb.k_scale), dev(hb.v_scale)
+    indptr, indices = dev(hb.pt.indptr), dev(hb.pt.indices)
+    tags, exp = dev(hb.pt.page_tags.view(np.int32)), dev(hb.pt.expected_tags.view(np.int32))
+    mask = torch.full((wl.batch,), 7, dtype=torch.uint8, device="cuda")
+    q = dev(hb.q, dtype=torch.bfloat16)
+    out = torch.empty(wl.batch, wl.num_q_heads, D, dtype=torch.bfloat16, device="cuda")
+    ws = fkv.alloc_workspace(wl.batch, wl.num_q_heads, Hkv)
+    rng = np.random.default_rng(77)
+    sm = 1.0 / np.sqrt(D)
+    fkv.device_error(clear=True)
+    for step in range(3):
+        kn = W.bf16_bits(rng.standard_normal((wl.batch, Hkv, D)).astype(np.float32))
+        vn = W.bf16_bits(rng.standard_normal((wl.batch, Hkv, D)).astype(np.float32))
+        fkv.kv_append_fp8_tag_check(dev(kn, dtype=torch.bfloat16), dev(vn, dtype=torch.bfloat16), dev(hb.slots_new),
+                                    ks, vs, kt, vt, tags, indptr, indices, exp, mask)
+        fkv.paged_decode_attn(q, kt, vt, indptr, indices, dev(hb.seq_lens), sm, out, ws, k_scale=ks, v_scale=vs,
+                              abort_mask=mask)
+        torch.cuda.synchronize()
+        orc.kv_append_fp8(kn, vn, hb.slots_new, hb.k_scale, hb.v_scale, kc, vc)
+        assert not mask.cpu().numpy().any()
+        ref = orc.paged_decode_attn(hb.q, kc, vc, hb.pt.indptr, hb.pt.indices, hb.seq_lens, sm,
+                                    k_scale=hb.k_scale, v_scale=hb.v_scale)
+        assert_close(bf16_out(out), ref, "step %d" % step)
+    assert np.array_equal(kt.cpu().numpy(), kc)
+    assert fkv.device_error() == 0
