@@ -256,15 +256,19 @@ class Step:
         self.fkv.kv_page_tag_check(self.page_tags, self.indptr, self.indices, self.expected, self.mask)
 
     def append_check(self, separate=False):
-        """The step's append and integrity check: one launch for an FP8 cache
-        (kv_append_fp8_tag_check), or the two calls one after the other."""
-        if self.fp8 and not separate:
+        """The step's append and integrity check: one launch
+        (kv_append_fp8_tag_check / kv_append_bf16_tag_check), or with
+        ``separate`` the two calls one after the other."""
+        if separate:
+            self.append()
+            self.check()
+        elif self.fp8:
             self.fkv.kv_append_fp8_tag_check(self.k_new, self.v_new, self.slots_new, self.k_scale, self.v_scale,
                                              self.k_cache, self.v_cache, self.page_tags, self.indptr, self.indices,
                                              self.expected, self.mask)
         else:
-            self.append()
-            self.check()
+            self.fkv.kv_append_bf16_tag_check(self.k_new, self.v_new, self.slots_new, self.k_cache, self.v_cache,
+                                              self.page_tags, self.indptr, self.indices, self.expected, self.mask)
 
     def attend(self, with_mask=True):
         self.fkv.paged_decode_attn(self.q, self.k_cache, self.v_cache, self.indptr, self.indices, self.seq_lens,
@@ -273,8 +277,7 @@ class Step:
                                    abort_mask=self.mask if with_mask else None)
 
     def launches_per_step(self, with_check=True):
-        prologue = 1 if (self.fp8 or not with_check) else 2          # append (+ check)
-        return prologue + self.fkv.kernels_per_call("paged_decode_attn")
+        return 1 + self.fkv.kernels_per_call("paged_decode_attn")   # append (+ check), attention
 
     def attn_bytes(self):
         """Algorithmic bytes of one paged_decode_attn call on the live requests
@@ -501,8 +504,7 @@ class Step:
                 fkv.kv_append_fp8_tag_check(kn, vn, sl, self.k_scale, self.v_scale, self.k_cache, self.v_cache,
                                             tags, indptr, ind, exp, mask)
             else:
-                fkv.kv_append_bf16(kn, vn, sl, self.k_cache, self.v_cache)
-                fkv.kv_page_tag_check(tags, indptr, ind, exp, mask)
+                fkv.kv_append_bf16_tag_check(kn, vn, sl, self.k_cache, self.v_cache, tags, indptr, ind, exp, mask)
             fkv.paged_decode_attn(q, self.k_cache, self.v_cache, indptr, ind, seq, self.sm, out, self.ws,
                                   k_scale=self.k_scale if self.fp8 else None,
                                   v_scale=self.v_scale if self.fp8 else None, abort_mask=mask)
@@ -650,8 +652,8 @@ def arm_config(wl, db, kv, world, attn_bytes):
     """The ``config`` of the JSON line, the same for both arms."""
     return {"workload": workload_text(wl, db), "kv_dtype": "fp8_e4m3" if kv == "fp8" else "bf16",
             "global_batch": world * wl.batch,
-            "step": ("kv_append_fp8_tag_check (append + integrity check, one launch)" if kv == "fp8" else
-                     "kv_append_bf16 + kv_page_tag_check") + " + paged_decode_attn (one layer)",
+            "step": "kv_append_%s_tag_check (append + integrity check, one launch) + paged_decode_attn (one layer)"
+                    % kv,
             "l2": "inputs larger than L2 (%.2f GB of KV read per step); no flush" % (attn_bytes / 1e9),
             "parallelism": "replicas x%d" % world}
 

@@ -11,6 +11,7 @@ Entry points (same names as the C ABI):
   kv_calibrate_scales              per-KV-head FP8 scales of a prompt (bulk write)
   kv_page_tag_check                the separate per-page generation-tag check
   kv_append_fp8_tag_check          the step's FP8 append and the tag check in one launch
+  kv_append_bf16_tag_check         the same for a BF16 cache
   kv_page_realloc                  bump tags (and optionally zero pages) of reallocated pages
   paged_decode_attn                decode attention over the paged cache
   paged_decode_attn_workspace_size bytes of scratch paged_decode_attn needs
@@ -23,7 +24,8 @@ import threading
 
 __all__ = [
     "FkvError", "KV_FP8_E4M3", "KV_BF16", "library_path", "load_library", "kv_append_fp8", "kv_append_bf16",
-    "kv_calibrate_scales", "kv_page_tag_check", "kv_append_fp8_tag_check", "kv_page_realloc", "paged_decode_attn",
+    "kv_calibrate_scales", "kv_page_tag_check", "kv_append_fp8_tag_check", "kv_append_bf16_tag_check", "kv_page_realloc",
+    "paged_decode_attn",
     "paged_decode_attn_workspace_size",
     "alloc_workspace",
     "paged_decode_attn_noalloc",
@@ -40,7 +42,7 @@ HEAD_DIM = 128
 
 EXPORTED_SYMBOLS = (
     "fkv_status_string", "kv_append_fp8", "kv_append_bf16", "kv_calibrate_scales", "kv_page_tag_check",
-    "kv_append_fp8_tag_check", "kv_page_realloc",
+    "kv_append_fp8_tag_check", "kv_append_bf16_tag_check", "kv_page_realloc",
     "paged_decode_attn_workspace_size", "paged_decode_attn", "paged_decode_attn_noalloc", "fkv_device_error",
     "fkv_kernels_per_call",
 )
@@ -87,6 +89,8 @@ def load_library():
         lib.kv_append_fp8_tag_check.restype = ctypes.c_int
         lib.kv_append_fp8_tag_check.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, i32, i32, P, P, P, P, i32, i64,
                                                 P, P]
+        lib.kv_append_bf16_tag_check.restype = ctypes.c_int
+        lib.kv_append_bf16_tag_check.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, P, P, P, P, i32, i64, P, P]
         lib.kv_calibrate_scales.restype = ctypes.c_int
         lib.kv_calibrate_scales.argtypes = [P, P, i64, i32, i32, P, P, P]
         lib.kv_page_realloc.restype = ctypes.c_int
@@ -219,6 +223,33 @@ def kv_append_fp8_tag_check(k_new, v_new, slot_mapping, k_scale, v_scale, k_cach
         _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), N, _ptr(k_scale), _ptr(v_scale), _ptr(k_cache),
         _ptr(v_cache), P, Hkv, S, D, _ptr(page_tags), _ptr(page_indptr), _ptr(page_indices), _ptr(expected_tags),
         B, page_indices.numel(), _ptr(abort_mask), _stream(stream)), "kv_append_fp8_tag_check")
+
+
+def kv_append_bf16_tag_check(k_new, v_new, slot_mapping, k_cache, v_cache,
+                             page_tags, page_indptr, page_indices, expected_tags, abort_mask, stream=None):
+    """``kv_append_bf16`` then ``kv_page_tag_check`` (same arguments, same
+    results) in one launch; ``page_tags`` has one entry per page of the pool."""
+    import torch
+    _dev(k_new, v_new, slot_mapping, k_cache, v_cache, page_tags, page_indptr, page_indices, expected_tags,
+         abort_mask)
+    _need(k_new.dtype == torch.bfloat16 and v_new.dtype == torch.bfloat16, "k_new/v_new must be bf16")
+    _need(k_cache.dtype == torch.bfloat16 and v_cache.dtype == torch.bfloat16, "BF16 caches expected")
+    _need(slot_mapping.dtype == torch.int64, "slot_mapping must be int64")
+    P, Hkv, S, D = k_cache.shape
+    _need(tuple(v_cache.shape) == (P, Hkv, S, D), "k_cache/v_cache shapes differ")
+    N = slot_mapping.numel()
+    _need(tuple(k_new.shape) == (N, Hkv, D) and tuple(v_new.shape) == (N, Hkv, D), "k_new/v_new shape")
+    _need(page_tags.dtype in (torch.uint32, torch.int32) and expected_tags.dtype == page_tags.dtype,
+          "tags must be 32-bit, both of one dtype")
+    _need(page_tags.numel() == P, "page_tags must have one entry per page of the pool")
+    _need(page_indptr.dtype == torch.int32 and page_indices.dtype == torch.int32, "CSR must be int32")
+    _need(abort_mask.dtype == torch.uint8, "abort_mask must be uint8")
+    B = page_indptr.numel() - 1
+    _need(abort_mask.numel() == B and expected_tags.numel() == page_indices.numel(), "size mismatch")
+    _raise(load_library().kv_append_bf16_tag_check(
+        _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), N, _ptr(k_cache), _ptr(v_cache), P, Hkv, S, D,
+        _ptr(page_tags), _ptr(page_indptr), _ptr(page_indices), _ptr(expected_tags), B, page_indices.numel(),
+        _ptr(abort_mask), _stream(stream)), "kv_append_bf16_tag_check")
 
 
 def kv_calibrate_scales(k, v, k_scale, v_scale, stream=None):

@@ -110,7 +110,7 @@ extern "C" int32_t fkv_kernels_per_call(const char *entry_point) {
     if (!entry_point) return -1;
     const std::string e(entry_point);
     if (e == "kv_append_fp8" || e == "kv_append_bf16" || e == "kv_page_tag_check" || e == "kv_page_realloc" ||
-        e == "kv_append_fp8_tag_check")
+        e == "kv_append_fp8_tag_check" || e == "kv_append_bf16_tag_check")
         return 1;
     if (e == "paged_decode_attn" || e == "paged_decode_attn_noalloc") return 2;   // plan, split attention
     if (e == "kv_calibrate_scales") return 2;                                     // amax, finalize

@@ -186,19 +186,17 @@ kv_append_fp8_tag_check_kernel(const uint4 *__restrict__ k_new, const uint4 *__r
                     page_size, page_shift, err, a % append_blocks_x, a / append_blocks_x);
 }
 
-__global__ void __launch_bounds__(kBlock)
-kv_append_bf16_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
-                      const int64_t *__restrict__ slots, int64_t n_tokens,
-                      uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
-                      int32_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t page_shift,
-                      uint32_t *err) {
-    grid_dep_wait();        // earlier readers of the pool (attention) have finished
-    grid_dep_launch();
+// One thread's share of the BF16 append in block (bx, by): the row copied
+// unchanged.
+__device__ __forceinline__ void append_bf16_part(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                                                 const int64_t *__restrict__ slots, int64_t n_tokens,
+                                                 uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                                                 int32_t num_pages, int32_t num_kv_heads, int32_t page_size,
+                                                 int32_t page_shift, uint32_t *err, unsigned bx, unsigned by) {
     int64_t dst_off = 0;
-    const int64_t n = locate(slots, n_tokens, num_pages, num_kv_heads, page_size, page_shift, err, blockIdx.x,
-                             blockIdx.y, dst_off);
+    const int64_t n = locate(slots, n_tokens, num_pages, num_kv_heads, page_size, page_shift, err, bx, by, dst_off);
     if (n < 0) return;
-    const int h = blockIdx.y;
+    const int h = by;
     const int sub = threadIdx.x % kThreadsPerToken;
     const bool is_v = sub >= kThreadsPerRow;
     const int chunk = sub % kThreadsPerRow;
@@ -207,6 +205,44 @@ kv_append_bf16_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__
     uint4 *dst = (is_v ? v_cache : k_cache) + dst_off / 8 + chunk * 2;
     dst[0] = r0;
     dst[1] = r1;
+}
+
+__global__ void __launch_bounds__(kBlock)
+kv_append_bf16_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                      const int64_t *__restrict__ slots, int64_t n_tokens,
+                      uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                      int32_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t page_shift,
+                      uint32_t *err) {
+    grid_dep_wait();        // earlier readers of the pool (attention) have finished
+    grid_dep_launch();
+    append_bf16_part(k_new, v_new, slots, n_tokens, k_cache, v_cache, num_pages, num_kv_heads, page_size,
+                     page_shift, err, blockIdx.x, blockIdx.y);
+}
+
+// The BF16 cache's step prologue in one launch, laid out like
+// kv_append_fp8_tag_check_kernel: check blocks first, then the append's.
+__global__ void __launch_bounds__(kBlock)
+kv_append_bf16_tag_check_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                                const int64_t *__restrict__ slots, int64_t n_tokens,
+                                uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                                int32_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t page_shift,
+                                uint32_t *err, unsigned append_blocks_x,
+                                const uint32_t *__restrict__ page_tags, const int32_t *__restrict__ page_indptr,
+                                const int32_t *__restrict__ page_indices,
+                                const uint32_t *__restrict__ expected_tags, int32_t batch, int64_t nnz,
+                                uint8_t *__restrict__ abort_mask) {
+    grid_dep_wait();        // earlier kernels' tags, tables and pool readers are done
+    grid_dep_launch();
+    const unsigned b = blockIdx.x;
+    if (b < static_cast<unsigned>(batch)) {
+        const int bad = tag_check_row<kBlock>(page_tags, num_pages, page_indptr, page_indices, expected_tags, nnz,
+                                              static_cast<int>(b));
+        if (threadIdx.x == 0) abort_mask[b] = bad ? 1 : 0;
+        return;
+    }
+    const unsigned a = b - static_cast<unsigned>(batch);
+    append_bf16_part(k_new, v_new, slots, n_tokens, k_cache, v_cache, num_pages, num_kv_heads, page_size,
+                     page_shift, err, a % append_blocks_x, a / append_blocks_x);
 }
 
 static fkv_status check_append_args(const void *k_new, const void *v_new, const int64_t *slot_mapping,
@@ -276,6 +312,29 @@ extern "C" fkv_status kv_append_bf16(const void *k_new, const void *v_new, const
     return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
 }
 
+// Argument checks of the one-launch append-and-check calls: those of the
+// append, then those of kv_page_tag_check; the grid's block count.
+static fkv_status check_combined_args(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                                      int32_t n_tokens, const void *k_cache, const void *v_cache,
+                                      int32_t num_pages, int32_t num_kv_heads, int32_t page_size,
+                                      int32_t head_dim, const uint32_t *page_tags, const int32_t *page_indptr,
+                                      const int32_t *page_indices, const uint32_t *expected_tags, int32_t batch,
+                                      int64_t nnz, uint8_t *abort_mask, int64_t &append_blocks_x,
+                                      int64_t &blocks) {
+    const fkv_status st = check_append_args(k_new, v_new, slot_mapping, n_tokens, k_cache, v_cache, num_pages,
+                                            num_kv_heads, page_size, head_dim);
+    if (st != FKV_OK) return st;
+    if (batch < 0 || nnz < 0) return FKV_ERR_INVALID_ARG;
+    if (batch > 0) {
+        if (!page_indptr || !abort_mask || !page_tags) return FKV_ERR_INVALID_ARG;
+        if (nnz > 0 && (!page_indices || !expected_tags)) return FKV_ERR_INVALID_ARG;
+    }
+    append_blocks_x = (static_cast<int64_t>(n_tokens) + kTokensPerBlock - 1) / kTokensPerBlock;
+    blocks = append_blocks_x * num_kv_heads + batch;
+    if (blocks > 0x7FFFFFFF) return FKV_ERR_UNSUPPORTED;
+    return FKV_OK;
+}
+
 extern "C" fkv_status kv_append_fp8_tag_check(const void *k_new, const void *v_new, const int64_t *slot_mapping,
                                               int32_t n_tokens, const float *k_scale, const float *v_scale,
                                               uint8_t *k_cache, uint8_t *v_cache, int32_t num_pages,
@@ -283,20 +342,13 @@ extern "C" fkv_status kv_append_fp8_tag_check(const void *k_new, const void *v_n
                                               const uint32_t *page_tags, const int32_t *page_indptr,
                                               const int32_t *page_indices, const uint32_t *expected_tags,
                                               int32_t batch, int64_t nnz, uint8_t *abort_mask, void *stream) {
-    fkv_status st = check_append_args(k_new, v_new, slot_mapping, n_tokens, k_cache, v_cache, num_pages,
-                                      num_kv_heads, page_size, head_dim);
+    int64_t gx = 0, blocks = 0;
+    const fkv_status st = check_combined_args(k_new, v_new, slot_mapping, n_tokens, k_cache, v_cache, num_pages,
+                                              num_kv_heads, page_size, head_dim, page_tags, page_indptr,
+                                              page_indices, expected_tags, batch, nnz, abort_mask, gx, blocks);
     if (st != FKV_OK) return st;
     if (n_tokens > 0 && (!k_scale || !v_scale)) return FKV_ERR_INVALID_ARG;
-    // the check's arguments, as kv_page_tag_check takes them
-    if (batch < 0 || nnz < 0) return FKV_ERR_INVALID_ARG;
-    if (batch > 0) {
-        if (!page_indptr || !abort_mask || !page_tags) return FKV_ERR_INVALID_ARG;
-        if (nnz > 0 && (!page_indices || !expected_tags)) return FKV_ERR_INVALID_ARG;
-    }
-    if (n_tokens == 0 && batch == 0) return FKV_OK;
-    const int64_t gx = (static_cast<int64_t>(n_tokens) + kTokensPerBlock - 1) / kTokensPerBlock;
-    const int64_t blocks = gx * num_kv_heads + batch;
-    if (blocks > 0x7FFFFFFF) return FKV_ERR_UNSUPPORTED;
+    if (blocks == 0) return FKV_OK;
     uint32_t *err = device_error_word();
     if (!err) return FKV_ERR_CUDA;
     const cudaError_t e = launch_pdl(kv_append_fp8_tag_check_kernel, dim3(static_cast<unsigned>(blocks)),
@@ -306,5 +358,29 @@ extern "C" fkv_status kv_append_fp8_tag_check(const void *k_new, const void *v_n
                                      v_cache, num_pages, num_kv_heads, page_size, page_shift_of(page_size), err,
                                      static_cast<unsigned>(gx > 0 ? gx : 1), page_tags, page_indptr, page_indices,
                                      expected_tags, batch, nnz, abort_mask);
+    return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
+}
+
+extern "C" fkv_status kv_append_bf16_tag_check(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                                               int32_t n_tokens, void *k_cache, void *v_cache, int32_t num_pages,
+                                               int32_t num_kv_heads, int32_t page_size, int32_t head_dim,
+                                               const uint32_t *page_tags, const int32_t *page_indptr,
+                                               const int32_t *page_indices, const uint32_t *expected_tags,
+                                               int32_t batch, int64_t nnz, uint8_t *abort_mask, void *stream) {
+    int64_t gx = 0, blocks = 0;
+    const fkv_status st = check_combined_args(k_new, v_new, slot_mapping, n_tokens, k_cache, v_cache, num_pages,
+                                              num_kv_heads, page_size, head_dim, page_tags, page_indptr,
+                                              page_indices, expected_tags, batch, nnz, abort_mask, gx, blocks);
+    if (st != FKV_OK) return st;
+    if (blocks == 0) return FKV_OK;
+    uint32_t *err = device_error_word();
+    if (!err) return FKV_ERR_CUDA;
+    const cudaError_t e = launch_pdl(kv_append_bf16_tag_check_kernel, dim3(static_cast<unsigned>(blocks)),
+                                     dim3(kBlock), 0, static_cast<cudaStream_t>(stream),
+                                     static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+                                     slot_mapping, static_cast<int64_t>(n_tokens), static_cast<uint4 *>(k_cache),
+                                     static_cast<uint4 *>(v_cache), num_pages, num_kv_heads, page_size,
+                                     page_shift_of(page_size), err, static_cast<unsigned>(gx > 0 ? gx : 1),
+                                     page_tags, page_indptr, page_indices, expected_tags, batch, nnz, abort_mask);
     return e == cudaSuccess ? FKV_OK : FKV_ERR_CUDA;
 }

@@ -185,6 +185,20 @@ FKV_API fkv_status kv_append_fp8_tag_check(const void *k_new, const void *v_new,
                                    int32_t batch, int64_t nnz, uint8_t *abort_mask, void *stream);
 
 /*
+ * kv_append_bf16_tag_check -- the same one-launch prologue for a BF16 cache:
+ * kv_append_bf16 followed by kv_page_tag_check, with the same arguments,
+ * results, argument checks and rules as kv_append_fp8_tag_check (no scales).
+ */
+FKV_API fkv_status kv_append_bf16_tag_check(const void *k_new, const void *v_new,
+                                    const int64_t *slot_mapping, int32_t n_tokens,
+                                    void *k_cache, void *v_cache,
+                                    int32_t num_pages, int32_t num_kv_heads,
+                                    int32_t page_size, int32_t head_dim,
+                                    const uint32_t *page_tags, const int32_t *page_indptr,
+                                    const int32_t *page_indices, const uint32_t *expected_tags,
+                                    int32_t batch, int64_t nnz, uint8_t *abort_mask, void *stream);
+
+/*
  * kv_page_realloc -- hand pages to new owners on the device ("Kimi and GLM
  * Reasoning Slimming: Hands-On Test", section "Giving Every Physical Cache
  * Page a 'Generation Number'": a page's tag changes each time it is

@@ -45,6 +45,7 @@ def test_library_loads_in_tree(lib_path):
     assert fkv.kernels_per_call("paged_decode_attn") == 2
     assert fkv.kernels_per_call("kv_page_tag_check") == 1
     assert fkv.kernels_per_call("kv_append_fp8_tag_check") == 1
+    assert fkv.kernels_per_call("kv_append_bf16_tag_check") == 1
 
 
 def test_host_validation_without_gpu(lib_path):
@@ -64,6 +65,12 @@ def test_host_validation_without_gpu(lib_path):
                                        None, None, None, None, 3, 0, None, None) == 1
     assert lib.kv_append_fp8_tag_check(None, None, None, 0, None, None, None, None, 4, 2, 16, 128,
                                        None, None, None, None, 0, 0, None, None) == 0
+    assert lib.kv_append_bf16_tag_check(None, None, None, 0, None, None, 4, 2, 16, 64,
+                                        None, None, None, None, 0, 0, None, None) == 2
+    assert lib.kv_append_bf16_tag_check(None, None, None, 0, None, None, 4, 2, 16, 128,
+                                        None, None, None, None, 3, 0, None, None) == 1
+    assert lib.kv_append_bf16_tag_check(None, None, None, 0, None, None, 4, 2, 16, 128,
+                                        None, None, None, None, 0, 0, None, None) == 0
     assert lib.paged_decode_attn(None, 2, 8, None, None, 0, None, None, 4, 2, 16, 64, None, None, 0, None, None,
                                  0.1, None, None, 0, None) == 2
     assert lib.paged_decode_attn(None, 2, 8, None, None, 0, None, None, 4, 2, 24, 128, None, None, 0, None, None,

@@ -1,6 +1,7 @@
-"""kv_append_fp8_tag_check on the GPU: the decode step's append and the
-integrity check in one launch give the oracle's pool bytes and abort mask bit
-for bit, and exactly what the two separate calls give."""
+"""kv_append_fp8_tag_check / kv_append_bf16_tag_check on the GPU: the
+decode step's append and the integrity check in one launch give the oracle's
+pool bytes and abort mask bit for bit, and exactly what the two separate
+calls give."""
 import numpy as np
 import pytest
 
@@ -24,12 +25,17 @@ def _tables(rng, P, B, faults=True):
     return tags, indptr, indices, expected
 
 
-def _run(orc, P, Hkv, S, N, B, seed, combined=True, faults=True):
+def _run(orc, P, Hkv, S, N, B, seed, combined=True, faults=True, kv="fp8"):
     import torch
     import fp8_paged_kv_decode_gb300 as fkv
     rng = np.random.default_rng(seed)
-    kc0 = rng.integers(0, 256, (P, Hkv, S, 128)).astype(np.uint8)
-    vc0 = rng.integers(0, 256, (P, Hkv, S, 128)).astype(np.uint8)
+    fp8 = kv == "fp8"
+    if fp8:
+        kc0 = rng.integers(0, 256, (P, Hkv, S, 128)).astype(np.uint8)
+        vc0 = rng.integers(0, 256, (P, Hkv, S, 128)).astype(np.uint8)
+    else:
+        kc0 = W.bf16_bits(rng.standard_normal((P, Hkv, S, 128)).astype(np.float32))
+        vc0 = W.bf16_bits(rng.standard_normal((P, Hkv, S, 128)).astype(np.float32))
     slots = rng.choice(P * S, size=N, replace=False).astype(np.int64) if N else np.zeros(0, np.int64)
     if N:
         slots[::13] = -1                                         # padding tokens
@@ -41,46 +47,55 @@ def _run(orc, P, Hkv, S, N, B, seed, combined=True, faults=True):
     # the oracle: append, then check
     kc, vc = kc0.copy(), vc0.copy()
     if N:
-        orc.kv_append_fp8(kb, vb, slots, ks, vs, kc, vc)
+        if fp8:
+            orc.kv_append_fp8(kb, vb, slots, ks, vs, kc, vc)
+        else:
+            orc.kv_append_bf16(kb, vb, slots, kc, vc)
     want_mask = orc.kv_page_tag_check(tags, indptr, indices, expected)
     # the GPU
-    kt, vt = dev(kc0), dev(vc0)
+    cdt = None if fp8 else torch.bfloat16
+    kt, vt = dev(kc0, dtype=cdt), dev(vc0, dtype=cdt)
     mask = torch.full((B,), 7, dtype=torch.uint8, device="cuda")
-    args = (dev(kb, dtype=torch.bfloat16) if N else torch.zeros(0, Hkv, 128, dtype=torch.bfloat16, device="cuda"),
-            dev(vb, dtype=torch.bfloat16) if N else torch.zeros(0, Hkv, 128, dtype=torch.bfloat16, device="cuda"),
-            dev(slots) if N else torch.zeros(0, dtype=torch.int64, device="cuda"), dev(ks), dev(vs), kt, vt)
+    new = (dev(kb, dtype=torch.bfloat16) if N else torch.zeros(0, Hkv, 128, dtype=torch.bfloat16, device="cuda"),
+           dev(vb, dtype=torch.bfloat16) if N else torch.zeros(0, Hkv, 128, dtype=torch.bfloat16, device="cuda"),
+           dev(slots) if N else torch.zeros(0, dtype=torch.int64, device="cuda"))
+    args = new + ((dev(ks), dev(vs)) if fp8 else ()) + (kt, vt)
     ind = dev(indices if indices.size else np.zeros(1, np.int32))[:indices.size]
     exp = dev(expected.view(np.int32) if expected.size else np.zeros(1, np.int32))[:expected.size]
     tg = dev(tags.view(np.int32))
     fkv.device_error(clear=True)
     if combined:
-        fkv.kv_append_fp8_tag_check(*args, tg, dev(indptr), ind, exp, mask)
+        (fkv.kv_append_fp8_tag_check if fp8 else fkv.kv_append_bf16_tag_check)(*args, tg, dev(indptr), ind, exp,
+                                                                               mask)
     else:
-        fkv.kv_append_fp8(*args)
+        (fkv.kv_append_fp8 if fp8 else fkv.kv_append_bf16)(*args)
         fkv.kv_page_tag_check(tg, dev(indptr), ind, exp, mask)
     torch.cuda.synchronize()
-    return kt.cpu().numpy(), vt.cpu().numpy(), mask.cpu().numpy(), kc, vc, want_mask
+    host = (lambda t: t.cpu().numpy()) if fp8 else (lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16))
+    return host(kt), host(vt), mask.cpu().numpy(), kc, vc, want_mask
 
 
+@pytest.mark.parametrize("kv", ["fp8", "bf16"])
 @pytest.mark.parametrize("P,Hkv,S,N,B", [(300, 8, 16, 256, 256), (64, 2, 64, 37, 5), (2000, 4, 32, 1000, 900),
                                          (50, 1, 128, 17, 1)])
-def test_combined_equals_oracle_and_separate_calls(orc, P, Hkv, S, N, B):
+def test_combined_equals_oracle_and_separate_calls(orc, P, Hkv, S, N, B, kv):
     import fp8_paged_kv_decode_gb300 as fkv
     seed = P + N + B
-    gk, gv, gm, kc, vc, want = _run(orc, P, Hkv, S, N, B, seed, combined=True)
+    gk, gv, gm, kc, vc, want = _run(orc, P, Hkv, S, N, B, seed, combined=True, kv=kv)
     assert np.array_equal(gk, kc) and np.array_equal(gv, vc), "pool bytes differ from the oracle"
     assert np.array_equal(gm, want), "abort mask differs from the oracle"
     assert want.any() or B == 1
-    sk, sv, sm, _, _, _ = _run(orc, P, Hkv, S, N, B, seed, combined=False)
+    sk, sv, sm, _, _, _ = _run(orc, P, Hkv, S, N, B, seed, combined=False, kv=kv)
     assert np.array_equal(gk, sk) and np.array_equal(gv, sv) and np.array_equal(gm, sm)
     assert fkv.device_error() == 0
 
 
-def test_check_only_and_append_only(orc):
+@pytest.mark.parametrize("kv", ["fp8", "bf16"])
+def test_check_only_and_append_only(orc, kv):
     """No tokens: the launch is the check alone.  An empty batch: the append alone."""
-    gk, gv, gm, kc, vc, want = _run(orc, 100, 2, 16, 0, 40, seed=9)
+    gk, gv, gm, kc, vc, want = _run(orc, 100, 2, 16, 0, 40, seed=9, kv=kv)
     assert np.array_equal(gk, kc) and np.array_equal(gv, vc) and np.array_equal(gm, want)
-    gk, gv, gm, kc, vc, want = _run(orc, 100, 2, 16, 60, 0, seed=10)
+    gk, gv, gm, kc, vc, want = _run(orc, 100, 2, 16, 60, 0, seed=10, kv=kv)
     assert np.array_equal(gk, kc) and np.array_equal(gv, vc) and gm.size == 0
 
 
@@ -118,9 +133,9 @@ def test_integrity_workload_step(orc):
 @pytest.mark.parametrize("seed", range(12))
 def test_fuzz_combined(orc, seed):
     """Random pool sizes, head counts, page sizes, token and request counts
-    and injected faults: the one-launch call matches the oracle and the two
-    separate calls bit for bit.  (Zero tokens or zero requests:
-    test_check_only_and_append_only.)"""
+    and injected faults (every fourth seed on a BF16 cache): the one-launch
+    call matches the oracle and the two separate calls bit for bit.  (Zero
+    tokens or zero requests: test_check_only_and_append_only.)"""
     rng = np.random.default_rng(900 + seed)
     S = int(rng.choice([16, 32, 64, 128]))
     Hkv = int(rng.choice([1, 2, 4, 8]))
@@ -129,10 +144,13 @@ def test_fuzz_combined(orc, seed):
     B = int(rng.integers(0, 300))
     if N == 0 and B == 0:
         B = 1
-    gk, gv, gm, kc, vc, want = _run(orc, P, Hkv, S, N, B, seed=1000 + seed, combined=True, faults=bool(seed % 3))
+    kv = "bf16" if seed % 4 == 3 else "fp8"
+    gk, gv, gm, kc, vc, want = _run(orc, P, Hkv, S, N, B, seed=1000 + seed, combined=True, faults=bool(seed % 3),
+                                    kv=kv)
     assert np.array_equal(gk, kc) and np.array_equal(gv, vc), "pool bytes differ from the oracle"
     assert np.array_equal(gm, want), "abort mask differs from the oracle"
-    sk, sv, sm, _, _, _ = _run(orc, P, Hkv, S, N, B, seed=1000 + seed, combined=False, faults=bool(seed % 3))
+    sk, sv, sm, _, _, _ = _run(orc, P, Hkv, S, N, B, seed=1000 + seed, combined=False, faults=bool(seed % 3),
+                               kv=kv)
     assert np.array_equal(gk, sk) and np.array_equal(gv, sv) and np.array_equal(gm, sm)
 
 
