@@ -404,26 +404,32 @@ class Step:
         del flush
         return float(np.median([a.elapsed_time(b) for a, b in ev]))
 
-    def time_prefill(self, reps=3):
+    def time_prefill(self, reps=5):
         """Bulk write of the whole cached context as a prefill would hand it
         over: kv_calibrate_scales on the bf16 prompt, then kv_append_fp8 of
-        every token (rewrites the same bytes)."""
+        every token (rewrites the same bytes).  Each call is timed in a run
+        of its own (median of ``reps`` after one untimed call): right after a
+        bulk append, a calibration first pays for writing back the append's
+        dirty L2 lines."""
         torch, fkv = self.torch, self.fkv
         db = self.db
         ks = torch.empty_like(self.k_scale)
         vs = torch.empty_like(self.v_scale)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        cal, app = [], []
-        for _ in range(reps + 1):
-            ev[0].record()
-            fkv.kv_calibrate_scales(db.k_src, db.v_src, ks, vs)
-            ev[1].record()
-            fkv.kv_append_fp8(db.k_src, db.v_src, db.slots_src, ks, vs, self.k_cache, self.v_cache)
-            ev[2].record()
-            torch.cuda.synchronize(self.device)
-            cal.append(ev[0].elapsed_time(ev[1]))
-            app.append(ev[1].elapsed_time(ev[2]))
-        cal_ms, app_ms = float(np.median(cal[1:])), float(np.median(app[1:]))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+        def run(call):
+            ts = []
+            for _ in range(reps + 1):
+                ev[0].record()
+                call()
+                ev[1].record()
+                torch.cuda.synchronize(self.device)
+                ts.append(ev[0].elapsed_time(ev[1]))
+            return float(np.median(ts[1:]))
+
+        cal_ms = run(lambda: fkv.kv_calibrate_scales(db.k_src, db.v_src, ks, vs))
+        app_ms = run(lambda: fkv.kv_append_fp8(db.k_src, db.v_src, db.slots_src, ks, vs, self.k_cache,
+                                               self.v_cache))
         ntok = int(db.slots_src.numel())
         src = 2 * ntok * self.Hkv * self.D * 2
         same = bool(torch.equal(ks, self.k_scale) and torch.equal(vs, self.v_scale))

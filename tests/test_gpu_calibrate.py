@@ -22,15 +22,21 @@ def _gpu_scales(kb, vb):
     return ks.cpu().numpy(), vs.cpu().numpy()
 
 
-@pytest.mark.parametrize("n", [0, 1, 17, 5000])
-def test_scales_bitexact(orc, n):
-    rng = np.random.default_rng(51 + n)
-    Hkv = 8
+@pytest.mark.parametrize("n,Hkv", [(0, 8), (1, 8), (17, 8), (5000, 8), (3, 1), (70000, 1), (4099, 2), (1, 4),
+                                   (9000, 4), (33, 16), (3000, 16), (500, 3), (2001, 5), (1000, 12)])
+def test_scales_bitexact(orc, n, Hkv):
+    """Head counts that divide the 16 rows of a block and ones that do not;
+    each head's maximum sits at a different token, the last head's at the
+    last token, and one head is all zeros."""
+    rng = np.random.default_rng(51 + n + 1000 * Hkv)
     kf = (rng.standard_normal((n, Hkv, 128)) * np.exp2(rng.integers(-6, 6, (1, Hkv, 1)))).astype(np.float32)
     vf = rng.standard_normal((n, Hkv, 128)).astype(np.float32)
     if n:
-        kf[:, 5, :] = 0.0
-        kf[n // 2, 1, 3] = 1.0e5
+        kf[:, Hkv // 2, :] = 0.0
+        for h in range(Hkv):
+            if h != Hkv // 2:
+                kf[(n - 1 - 7 * h) % n, h, (5 * h) % 128] = 1.0e5 * (h + 1)
+        vf[n - 1, Hkv - 1, 127] = -3.0e4
     kb, vb = W.bf16_bits(kf), W.bf16_bits(vf)
     gk, gv = _gpu_scales(kb, vb)
     ok, ov = orc.kv_calibrate_scales(kb, vb)
