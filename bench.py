@@ -771,7 +771,7 @@ def config_table(device, rank, reps, warmup, peak, reuse=None):
         key = name if stale is None else "%s_stale%g" % (name, stale)
         if stale is not None:
             wl = dataclasses.replace(wl, name=key, stale_frac=stale)
-        db = reuse if (reuse is not None and stale is None and reuse.wl.name == name) else \
+        db = reuse if (reuse is not None and stale is None and reuse.wl == wl) else \
             W.device_batch(wl, device, seed=wl.seed + rank)
         st = Step(db, kv, device)
         st.check()                                   # the abort mask the timed calls read
@@ -863,7 +863,7 @@ def capacity_rows(db, device, steps, warmup):
     budget = int(npages[:32].sum()) * page_bf16
     adm = {"fp8": W.admitted(page_fp8, npages, budget), "bf16": W.admitted(page_bf16, npages, budget)}
     rows = []
-    for c in sorted({1, 2, 4, 8, 16, 32, 48, 64, adm["fp8"], adm["bf16"]} - {0}):
+    for c in sorted({c for c in (1, 2, 4, 8, 16, 32, 48, 64, adm["fp8"], adm["bf16"]) if 0 < c <= npages.size}):
         row = {"requests": c, "tokens": int(db.seq_lens[:c].sum())}
         sub = W.subset_batch(db, c)
         for kv in ("fp8", "bf16"):
@@ -1094,7 +1094,11 @@ def main():
                                        args.warmup, peak, reuse=db)
         del fp8
         torch.cuda.empty_cache()
-        line["capacity_sweep"] = capacity_rows(db, device, max(50, args.steps // 10), args.warmup)
+        # the sweep is defined on the headline workload as drawn; another
+        # selected workload (or batch / page-size change) gets its own batch
+        cdb = db if db.wl == W.WORKLOADS[HEADLINE] else W.device_batch(W.WORKLOADS[HEADLINE], device)
+        line["capacity_sweep"] = capacity_rows(cdb, device, max(50, args.steps // 10), args.warmup)
+        del cdb
 
     derr = fkv.device_error()
     if derr:

@@ -364,7 +364,8 @@ def compact_requests(db: DeviceBatch, reqs) -> CompactRequests:
 
 def subset_batch(db: DeviceBatch, n: int) -> DeviceBatch:
     """The first ``n`` requests of a batch, same pool and page ids."""
-    import torch
+    if not 0 <= n <= db.wl.batch:
+        raise ValueError("subset of %d requests from a batch of %d" % (n, db.wl.batch))
     pt = db.pt
     nnz = int(pt.indptr[n])
     ntok = int(db.ctx[:n].sum())

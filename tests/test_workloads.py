@@ -129,3 +129,16 @@ def test_share_prefix_rewrites_only_long_requests():
     np.testing.assert_array_equal(sp.indices[13:16], pt.indices[:3])   # request 3
     np.testing.assert_array_equal(sp.indices[16:], pt.indices[16:])
     np.testing.assert_array_equal(sp.expected_tags[13:16], pt.expected_tags[:3])
+
+
+def test_subset_batch_keeps_the_first_requests():
+    db = W.device_batch(W.WORKLOADS["tiny_gqa4"], "cpu")
+    sub = W.subset_batch(db, 2)
+    assert sub.wl.batch == 2
+    np.testing.assert_array_equal(sub.seq_lens, db.seq_lens[:2])
+    np.testing.assert_array_equal(sub.pt.indptr, db.pt.indptr[:3])
+    np.testing.assert_array_equal(sub.pt.indices, db.pt.indices[:db.pt.indptr[2]])
+    assert sub.k_src.shape[0] == int(db.ctx[:2].sum())
+    assert W.subset_batch(db, 0).wl.batch == 0
+    with pytest.raises(ValueError):
+        W.subset_batch(db, db.wl.batch + 1)
