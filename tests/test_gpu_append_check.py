@@ -198,3 +198,49 @@ def test_small_integrity_step_after_one_launch_prologue(orc):
         assert_close(bf16_out(out), ref, "step %d" % step)
     assert np.array_equal(kt.cpu().numpy(), kc)
     assert fkv.device_error() == 0
+
+
+@pytest.mark.parametrize("nnz", [0, 1, 255, 256, 511, 1023, 1024, 1025, 2047, 2048, 2049, 3000])
+def test_small_tables_with_malformed_rows(orc, nnz):
+    """Page tables of up to 8 requests whose sizes straddle multiples of the
+    check blocks' strides (128 and 256 threads, four entries in flight each):
+    masks of the stand-alone check and of the append-and-check launch equal
+    the oracle's, with stale tags, ids outside the pool, a row whose bounds
+    are reversed, and a last row that ends past the entries passed."""
+    import torch
+    import fp8_paged_kv_decode_gb300 as fkv
+    rng = np.random.default_rng(7000 + nnz)
+    P = 97
+    B = int(rng.integers(1, 9))
+    cuts = np.sort(rng.integers(0, nnz + 1, B - 1)) if B > 1 else np.zeros(0, np.int64)
+    indptr = np.concatenate([[0], cuts, [nnz]]).astype(np.int32)
+    tags = rng.integers(0, 2 ** 32, P, dtype=np.uint64).astype(np.uint32)
+    indices = rng.integers(0, P, nnz).astype(np.int32)
+    expected = tags[indices].copy()
+    if nnz:
+        j = rng.integers(0, nnz, 3)
+        expected[j[0]] += np.uint32(1)                       # stale
+        indices[j[1]] = P + 1                                # outside the pool
+    variants = [("as drawn", indptr, indices, expected)]
+    if B >= 3:
+        bad = indptr.copy()
+        bad[1] = bad[2] + 1                                  # row 0 ends after row 1 starts: row 1 reversed
+        variants.append(("reversed row", bad, indices, expected))
+    if nnz >= 2:
+        variants.append(("last row past the entries", indptr, indices[:nnz - 1], expected[:nnz - 1]))
+    for what, ip, ind_h, exp_h in variants:
+        want = orc.kv_page_tag_check(tags, ip, ind_h, exp_h)
+        tg = dev(tags.view(np.int32))
+        ind = dev(ind_h if ind_h.size else np.zeros(1, np.int32))[:ind_h.size]
+        exp = dev(exp_h.view(np.int32) if exp_h.size else np.zeros(1, np.int32))[:exp_h.size]
+        m1 = torch.full((B,), 7, dtype=torch.uint8, device="cuda")
+        m2 = torch.full((B,), 7, dtype=torch.uint8, device="cuda")
+        fkv.kv_page_tag_check(tg, dev(ip), ind, exp, m1)
+        kc = torch.zeros((P, 1, 16, 128), dtype=torch.uint8, device="cuda")
+        none_bf = torch.zeros(0, 1, 128, dtype=torch.bfloat16, device="cuda")
+        one = torch.ones(1, dtype=torch.float32, device="cuda")
+        fkv.kv_append_fp8_tag_check(none_bf, none_bf, torch.zeros(0, dtype=torch.int64, device="cuda"), one, one,
+                                    kc, kc.clone(), tg, dev(ip), ind, exp, m2)
+        torch.cuda.synchronize()
+        assert np.array_equal(m1.cpu().numpy(), want), (what, "stand-alone check")
+        assert np.array_equal(m2.cpu().numpy(), want), (what, "append-and-check launch")
