@@ -102,18 +102,11 @@ constexpr int kMinAlignedTiles = FKV_ALIGNED_MIN_TILES;
 #ifndef FKV_LOCAL_PLAN_MAX
 #define FKV_LOCAL_PLAN_MAX 128
 #endif
-// At the end of its range a warp holding the last unfinished part of a unit
-// merges from its registers (1) instead of publishing its part and merging
-// through the stage ring (0).
+// At the end of its range a warp holding the first part of a unit of at most
+// three parts, whose other parts have all arrived, merges from its registers
+// (1) instead of publishing its part and arriving (0).
 #ifndef FKV_TRY_LAST
 #define FKV_TRY_LAST 1
-#endif
-// A warp that becomes the last of a unit's parts in the middle of its range
-// (the tail of the unit it started in) records the merge and performs it at
-// its range end through the idle stage ring (1), instead of stalling its
-// stream for a merge through registers there (0).
-#ifndef FKV_DEFER_MIDRANGE
-#define FKV_DEFER_MIDRANGE 1
 #endif
 constexpr int kLocalPlanMax = FKV_LOCAL_PLAN_MAX;
 static_assert(kLocalPlanMax <= 1024, "one 32-request chunk per lane");
@@ -487,130 +480,11 @@ __device__ __forceinline__ int64_t warp_of_tile(int64_t x, int64_t T, int NW) {
 
 // Merge n partials stored at slots slot0, slot0 + stride, ... into either the
 // final bf16 rows of unit (r, h) (scaled by vsc / L) or one fp32 partial
-// written to slot `dst` (the first level of a two-level merge).  With
-// `maybe_empty` (tiles < warps) entries of warps with an empty range, which
-// wrote nothing, are skipped; entry j belongs to warp wk0 + j.
-//
-// Latency matters more than bandwidth here (a few KB per entry), so the
-// statistics of up to 32 entries come in one round of loads (lane = entry,
-// all heads per lane) and the output pass keeps two entries' loads (all heads,
-// 4 dims per lane) in flight.
-__device__ void merge_parts(const AttnParams &p, int nw, int64_t slot0, int n, int stride, bool maybe_empty,
-                            int64_t wk0, int64_t T, bool final_out, int r, int h, float vsc, int64_t dst) {
-    const int lane = threadIdx.x & 31;
-    const int G = p.G;
-    auto empty = [&](int j) {
-        return maybe_empty && warp_lo(wk0 + j, T, nw) == warp_lo(wk0 + j + 1, T, nw);
-    };
-    auto slot_of = [&](int j) { return slot0 + static_cast<int64_t>(j) * stride; };
-    // statistics: per-head max, invalid flag, then normaliser
-    float M[kMaxGroup], L[kMaxGroup];
-#pragma unroll
-    for (int hd = 0; hd < kMaxGroup; ++hd) {
-        M[hd] = -INFINITY;
-        L[hd] = 0.f;
-    }
-    bool bad = false;
-    for (int k0 = 0; k0 < n; k0 += 32) {
-        const int k = k0 + lane;
-        if (k < n && !empty(k)) {
-#pragma unroll
-            for (int hd = 0; hd < kMaxGroup; ++hd) {
-                if (hd >= G) break;
-                const float2 ml = __ldcg(p.part_ml + slot_of(k) * p.GP + hd);
-                bad |= ml.y < 0.f;
-                M[hd] = fmaxf(M[hd], ml.x);
-            }
-        }
-    }
-#pragma unroll
-    for (int hd = 0; hd < kMaxGroup; ++hd)
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) M[hd] = fmaxf(M[hd], __shfl_xor_sync(kFull, M[hd], o));
-    bad = __any_sync(kFull, bad);
-    float F[kMaxGroup];                                  // this lane's entry weights (first 32 entries)
-#pragma unroll
-    for (int hd = 0; hd < kMaxGroup; ++hd) F[hd] = 0.f;
-    for (int k0 = 0; k0 < n; k0 += 32) {
-        const int k = k0 + lane;
-        if (k < n && !empty(k)) {
-#pragma unroll
-            for (int hd = 0; hd < kMaxGroup; ++hd) {
-                if (hd >= G) break;
-                const float2 ml = __ldcg(p.part_ml + slot_of(k) * p.GP + hd);
-                const float f = ex2(ml.x - M[hd]);
-                L[hd] += f * ml.y;
-                if (k0 == 0) F[hd] = f;
-            }
-        }
-    }
-#pragma unroll
-    for (int hd = 0; hd < kMaxGroup; ++hd)
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) L[hd] += __shfl_xor_sync(kFull, L[hd], o);
-    // weighted sum of the entries' outputs, 4 dims per lane, two entries in flight
-    float4 acc[kMaxGroup];
-#pragma unroll
-    for (int hd = 0; hd < kMaxGroup; ++hd) acc[hd] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (!bad) {
-        for (int k = 0; k < n; k += 2) {
-            float fw[2][kMaxGroup];
-            float4 v[2][kMaxGroup];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int j = k + e;
-                const bool live = j < n && !empty(j);
-#pragma unroll
-                for (int hd = 0; hd < kMaxGroup; ++hd) {
-                    float f = 0.f;
-                    if (j < 32) {
-                        f = __shfl_sync(kFull, F[hd], j & 31);
-                    } else if (live && hd < G) {         // entries past the first 32: reload
-                        const float2 ml = __ldcg(p.part_ml + slot_of(j) * p.GP + hd);
-                        f = ex2(ml.x - M[hd]);
-                    }
-                    fw[e][hd] = (live && hd < G) ? f : 0.f;
-                    v[e][hd] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (fw[e][hd] > 0.f)
-                        v[e][hd] = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (slot_of(j) * G + hd) * kD) + lane);
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-#pragma unroll
-                for (int hd = 0; hd < kMaxGroup; ++hd) {
-                    acc[hd].x += fw[e][hd] * v[e][hd].x;
-                    acc[hd].y += fw[e][hd] * v[e][hd].y;
-                    acc[hd].z += fw[e][hd] * v[e][hd].z;
-                    acc[hd].w += fw[e][hd] * v[e][hd].w;
-                }
-        }
-    }
-    if (final_out) {
-#pragma unroll
-        for (int hd = 0; hd < kMaxGroup; ++hd) {
-            if (hd >= G) break;
-            const float sc = bad ? 0.f : vsc / L[hd];
-            uint2 *orow =
-                reinterpret_cast<uint2 *>(p.out + (static_cast<int64_t>(r) * p.Hq + h * G + hd) * kD) + lane;
-            *orow = make_uint2(pack_bf16x2(acc[hd].x * sc, acc[hd].y * sc),
-                               pack_bf16x2(acc[hd].z * sc, acc[hd].w * sc));
-        }
-    } else {
-#pragma unroll
-        for (int hd = 0; hd < kMaxGroup; ++hd) {
-            if (hd >= G) break;
-            __stcg(reinterpret_cast<float4 *>(p.part_o + (dst * G + hd) * kD) + lane, acc[hd]);
-        }
-#pragma unroll
-        for (int hd = 0; hd < kMaxGroup; ++hd)
-            if (hd < G && lane == hd) __stcg(p.part_ml + dst * p.GP + hd, make_float2(M[hd], bad ? -1.f : L[hd]));
-    }
-}
-
-// The same merge with the partials fetched into shared memory first, for a
-// warp whose stage ring is idle (the end of its range).  Each entry arrives in
-// two bulk copies (outputs, statistics) issued by the lane that owns it, all
+// written to slot `dst` (the first level of a two-level merge), for a warp
+// whose stage ring is idle (the end of its range).  With `maybe_empty`
+// (tiles < warps) entries of warps with an empty range, which wrote nothing,
+// are skipped; entry j belongs to warp wk0 + j.  Each entry arrives in two
+// bulk copies (outputs, statistics) issued by the lane that owns it, all
 // completing on `bar`, so a batch of up to `cap` (<= 32) entries costs one
 // memory round trip.  The statistics are reduced across lanes (one entry per
 // lane); each entry's weights go to shared memory and the output pass reads
@@ -619,6 +493,17 @@ __device__ void merge_parts(const AttnParams &p, int nw, int64_t slot0, int n, i
 // acquire-release arrival after the writers' own); the proxy fence carries
 // that to the bulk copies.  Returns false if a batch's copies did not land in
 // time; nothing is written then.
+//
+// The arithmetic of one batch is the merge's definition, which the register
+// merge at a range end reproduces exactly (merge_regs): with the live entries
+// packed in index order at lanes 0, 1, ..., per head
+//     M = max_e m_e,   w_e = 2^(m_e - M),
+//     L = the xor-butterfly sum over the 32 lanes of RN(w_e l_e) (0 past the entries),
+//     acc = fma(w_{n-1}, o_{n-1}, ... fma(w_1, o_1, fma(w_0, o_0, 0))),
+//     row = bf16(RN(acc RN(vsc / L))), or zeros if any entry is marked bad,
+// every rounding explicit (_rn operations, nothing left to contraction), so
+// a row's bytes do not depend on which warp merges it, on which of the two
+// paths it takes, or on when the parts arrive.
 __device__ bool merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, uint32_t bar, uint32_t &phase, int nw,
                                  int64_t slot0, int n, int stride, bool maybe_empty, int64_t wk0, int64_t T,
                                  bool final_out, int r, int h, float vsc, int64_t dst) {
@@ -644,7 +529,7 @@ __device__ bool merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, ui
         const uint32_t lmask = __ballot_sync(kFull, live);
         const int nv = __popc(lmask);
         if (nv == 0) continue;
-        const uint32_t pos = __popc(lmask & ((1u << lane) - 1u));   // live entries are packed
+        const uint32_t pos = __popc(lmask & ((1u << lane) - 1u));   // live entries are packed, in order
         if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nv) * (obytes + mbytes));
         __syncwarp();
         if (live) {
@@ -682,14 +567,14 @@ __device__ bool merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, ui
             mb = fmaxf(mb, M[hd]);
             const float f = M[hd] == -INFINITY ? 0.f : ex2(M[hd] - mb);
             wv[hd] = mv[hd] == -INFINITY ? 0.f : ex2(mv[hd] - mb);
-            float sl = wv[hd] * lv[hd];
+            float sl = __fmul_rn(wv[hd], lv[hd]);
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) sl += __shfl_xor_sync(kFull, sl, o);
-            L[hd] = L[hd] * f + sl;
-            acc[hd].x *= f;
-            acc[hd].y *= f;
-            acc[hd].z *= f;
-            acc[hd].w *= f;
+            for (int o = 1; o < 32; o <<= 1) sl = __fadd_rn(sl, __shfl_xor_sync(kFull, sl, o));
+            L[hd] = __fmaf_rn(L[hd], f, sl);
+            acc[hd].x = __fmul_rn(acc[hd].x, f);
+            acc[hd].y = __fmul_rn(acc[hd].y, f);
+            acc[hd].z = __fmul_rn(acc[hd].z, f);
+            acc[hd].w = __fmul_rn(acc[hd].w, f);
             M[hd] = mb;
         }
         if (lane < nv) {
@@ -705,10 +590,10 @@ __device__ bool merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, ui
             for (int hd = 0; hd < kMaxGroup; ++hd) {
                 if (hd < G) {
                     const float4 v = ld_shared_f4(sbuf + e * obytes + hd * (kD * 4) + lane * 16);
-                    acc[hd].x += wgt[hd] * v.x;
-                    acc[hd].y += wgt[hd] * v.y;
-                    acc[hd].z += wgt[hd] * v.z;
-                    acc[hd].w += wgt[hd] * v.w;
+                    acc[hd].x = __fmaf_rn(wgt[hd], v.x, acc[hd].x);
+                    acc[hd].y = __fmaf_rn(wgt[hd], v.y, acc[hd].y);
+                    acc[hd].z = __fmaf_rn(wgt[hd], v.z, acc[hd].z);
+                    acc[hd].w = __fmaf_rn(wgt[hd], v.w, acc[hd].w);
                 }
             }
         }
@@ -719,12 +604,12 @@ __device__ bool merge_parts_smem(const AttnParams &p, uint32_t sbuf, int cap, ui
 #pragma unroll
         for (int hd = 0; hd < kMaxGroup; ++hd) {
             if (hd >= G) break;
-            const float sc = vsc / L[hd];
+            const float sc = __fdiv_rn(vsc, L[hd]);
             uint2 *orow =
                 reinterpret_cast<uint2 *>(p.out + (static_cast<int64_t>(r) * p.Hq + h * G + hd) * kD) + lane;
             *orow = bad ? make_uint2(0u, 0u)
-                        : make_uint2(pack_bf16x2(acc[hd].x * sc, acc[hd].y * sc),
-                                     pack_bf16x2(acc[hd].z * sc, acc[hd].w * sc));
+                        : make_uint2(pack_bf16x2(__fmul_rn(acc[hd].x, sc), __fmul_rn(acc[hd].y, sc)),
+                                     pack_bf16x2(__fmul_rn(acc[hd].z, sc), __fmul_rn(acc[hd].w, sc)));
         }
     } else {
 #pragma unroll
@@ -984,13 +869,10 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     };
     // A merge this warp owes (kFinalDue: the single-level merge of a unit;
     // kChunkDue: the first level of a two-level merge, then the unit's
-    // arrival and, if last, its second level), for unit (r, h).
-    auto merge_steps = [&](int stage, const UnitGeom &gm, int r, int h, float vsc, bool ring) {
+    // arrival and, if last, its second level), for unit (r, h), performed at
+    // the end of the warp's range, where the stage ring is idle.
+    auto merge_steps = [&](int stage, const UnitGeom &gm, int r, int h, float vsc) {
         auto merge = [&](int64_t sl0, int cnt, int stride, bool me, int64_t wk0, bool fin, int64_t d) {
-            if (!ring) {
-                merge_parts(p, nw, sl0, cnt, stride, me, wk0, T, fin, r, h, vsc, d);
-                return true;
-            }
             if (merge_parts_smem(p, sbase, merge_cap, merge_bar, merge_phase, nw, sl0, cnt, stride, me, wk0, T,
                                  fin, r, h, vsc, d))
                 return true;
@@ -1023,13 +905,11 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
     bool unit_bad = false;
     float cvsc = 1.f;       // the unit's V scale
     UnitGeom cgm = agm;     // where the unit's parts sit, if it is split (span 0: not yet known)
-#if FKV_DEFER_MIDRANGE
     // a merge this warp owes from the middle of its range: at most one, since
     // only the unit it started in can end there and be split
     int def_stage = kNone, def_r = 0, def_h = 0;
     UnitGeom def_gm{0, 0};
     float def_vsc = 1.f;
-#endif
 
     for (int64_t i = 0; i < n_tiles; ++i) {
         const int s = static_cast<int>(i % NST);
@@ -1329,83 +1209,114 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                 return n;
             };
             // The unit's final merge from this warp's registers plus the other
-            // parts' partials, loaded straight from L2 (one round trip per
-            // part), written as the bf16 row.  The caller has acquired every
-            // other part.
+            // parts' partials (at most two), loaded straight from L2: their
+            // statistics and the first one's outputs in one round trip, the
+            // second one's outputs in another.  This warp holds the unit's
+            // first part, so its registers are entry 0 of merge_parts_smem's
+            // definition and the other parts follow in index order; every
+            // step below is that definition's, with the same roundings, so the
+            // row's bytes equal those of the merge through the stage ring.
+            // The caller has acquired every other part.
             auto merge_regs = [&](int64_t u) {
                 const int d0 = kFp8 ? 16 * g : 8 * g, d1 = kFp8 ? 16 * g + 8 : 64 + 8 * g;
-                float v[2][16], Mj[2], Lj[2];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-#pragma unroll
-                    for (int a = 0; a < 8; ++a) {
-                        v[j][2 * a] = o[a][j];
-                        v[j][2 * a + 1] = o[a][2 + j];
-                    }
-                    Mj[j] = m[j];
-                    Lj[j] = lt[j];
-                }
-                bool bad = unit_bad;
+                int64_t x0 = 0, x1 = 0;                       // the other parts, in index order
+                int no = 0;
                 for (int64_t x = cgm.wf; x < cgm.wf + cgm.span; ++x) {
                     if (x == w || (maybe_empty && warp_lo(x, T, nw) == warp_lo(x + 1, T, nw))) continue;
-                    const int64_t slot = u + x;
-                    // both heads' loads of this part go out together (one round trip);
-                    // lanes past the group's heads read a valid row and drop it
-                    float2 ml[2];
-                    float4 q[2][4];
+                    if (no == 0) x0 = x;
+                    else x1 = x;
+                    ++no;
+                }
+                // lanes past the group's heads read a valid row and drop it
+                float2 ml[2][2];
+                float4 q[2][4];
+                auto load_rows = [&](int k) {
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const int hd = min(2 * t + j, G - 1);
-                        const float4 *prow = reinterpret_cast<const float4 *>(p.part_o + (slot * G + hd) * kD);
-                        ml[j] = __ldcg(p.part_ml + slot * p.GP + hd);
+                        const float4 *prow =
+                            reinterpret_cast<const float4 *>(p.part_o + ((u + (k ? x1 : x0)) * G + hd) * kD);
                         q[j][0] = __ldcg(prow + d0 / 4);
                         q[j][1] = __ldcg(prow + d0 / 4 + 1);
                         q[j][2] = __ldcg(prow + d1 / 4);
                         q[j][3] = __ldcg(prow + d1 / 4 + 1);
                     }
+                };
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        ml[k][j] = k < no ? __ldcg(p.part_ml + (u + (k ? x1 : x0)) * p.GP + min(2 * t + j, G - 1))
+                                          : make_float2(-INFINITY, 0.f);
+                load_rows(0);
+                bool bad = unit_bad;
+                float v[2][16], w1[2], w2[2], Lj[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    bad |= ml[0][j].y < 0.f || ml[1][j].y < 0.f;
+                    const float mx = fmaxf(fmaxf(m[j], ml[0][j].x), ml[1][j].x);
+                    const float w0 = m[j] == -INFINITY ? 0.f : ex2(m[j] - mx);
+                    w1[j] = ml[0][j].x == -INFINITY ? 0.f : ex2(ml[0][j].x - mx);
+                    w2[j] = ml[1][j].x == -INFINITY ? 0.f : ex2(ml[1][j].x - mx);
+                    // the lanes' butterfly sum with entries at lanes 0, 1, 2 (zeros past them)
+                    const float sl = __fadd_rn(__fadd_rn(__fmul_rn(w0, lt[j]), __fmul_rn(w1[j], ml[0][j].y)),
+                                               __fmul_rn(w2[j], ml[1][j].y));
+                    Lj[j] = __fmaf_rn(0.f, 0.f, sl);
+#pragma unroll
+                    for (int a = 0; a < 8; ++a) {
+                        v[j][2 * a] = __fmaf_rn(w0, o[a][j], 0.f);
+                        v[j][2 * a + 1] = __fmaf_rn(w0, o[a][2 + j], 0.f);
+                    }
+                }
+                for (int k = 0; k < no; ++k) {
+                    if (k == 1) load_rows(1);
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const float qv[16] = {q[j][0].x, q[j][0].y, q[j][0].z, q[j][0].w, q[j][1].x, q[j][1].y,
                                               q[j][1].z, q[j][1].w, q[j][2].x, q[j][2].y, q[j][2].z, q[j][2].w,
                                               q[j][3].x, q[j][3].y, q[j][3].z, q[j][3].w};
-                        bad |= ml[j].y < 0.f;
-                        const float Mn = fmaxf(Mj[j], ml[j].x);
-                        const float a = ex2(Mj[j] - Mn), b = ex2(ml[j].x - Mn);
-                        Lj[j] = Lj[j] * a + ml[j].y * b;
+                        const float wk = k == 0 ? w1[j] : w2[j];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) v[j][e] = v[j][e] * a + qv[e] * b;
-                        Mj[j] = Mn;
+                        for (int e = 0; e < 16; ++e) v[j][e] = __fmaf_rn(wk, qv[e], v[j][e]);
                     }
                 }
+                bad = __any_sync(kFull, bad);
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int hd = 2 * t + j;
                     if (hd >= G) continue;
-                    const float f = bad ? 0.f : cvsc / Lj[j];
+                    const float f = __fdiv_rn(cvsc, Lj[j]);
                     __nv_bfloat16 *orow = p.out + (static_cast<int64_t>(C.r) * p.Hq + C.h * G + hd) * kD;
-                    uint4 r0v, r1v;
-                    r0v.x = pack_bf16x2(v[j][0] * f, v[j][1] * f);
-                    r0v.y = pack_bf16x2(v[j][2] * f, v[j][3] * f);
-                    r0v.z = pack_bf16x2(v[j][4] * f, v[j][5] * f);
-                    r0v.w = pack_bf16x2(v[j][6] * f, v[j][7] * f);
-                    r1v.x = pack_bf16x2(v[j][8] * f, v[j][9] * f);
-                    r1v.y = pack_bf16x2(v[j][10] * f, v[j][11] * f);
-                    r1v.z = pack_bf16x2(v[j][12] * f, v[j][13] * f);
-                    r1v.w = pack_bf16x2(v[j][14] * f, v[j][15] * f);
+                    uint4 r0v = make_uint4(0u, 0u, 0u, 0u), r1v = make_uint4(0u, 0u, 0u, 0u);
+                    if (!bad) {                                // fail closed: zeros, whatever the data
+                        r0v.x = pack_bf16x2(__fmul_rn(v[j][0], f), __fmul_rn(v[j][1], f));
+                        r0v.y = pack_bf16x2(__fmul_rn(v[j][2], f), __fmul_rn(v[j][3], f));
+                        r0v.z = pack_bf16x2(__fmul_rn(v[j][4], f), __fmul_rn(v[j][5], f));
+                        r0v.w = pack_bf16x2(__fmul_rn(v[j][6], f), __fmul_rn(v[j][7], f));
+                        r1v.x = pack_bf16x2(__fmul_rn(v[j][8], f), __fmul_rn(v[j][9], f));
+                        r1v.y = pack_bf16x2(__fmul_rn(v[j][10], f), __fmul_rn(v[j][11], f));
+                        r1v.z = pack_bf16x2(__fmul_rn(v[j][12], f), __fmul_rn(v[j][13], f));
+                        r1v.w = pack_bf16x2(__fmul_rn(v[j][14], f), __fmul_rn(v[j][15], f));
+                    }
                     *reinterpret_cast<uint4 *>(orow + d0) = r0v;
                     *reinterpret_cast<uint4 *>(orow + d1) = r1v;
                 }
             };
             bool merged = false;
 #if FKV_TRY_LAST
-            if (!whole && i == n_tiles - 1 && (maybe_empty || cgm.span <= kChunk)) {
-                // The unit's other parts usually end early in their warps'
-                // ranges, so at this warp's range end they may all have
-                // arrived.  Then this warp is the last: it merges its registers
-                // with their partials, loaded straight from global memory
-                // (one round trip for a unit over two warps), and writes the
-                // row -- no partial of its own, no arrival.  Otherwise it
-                // publishes and arrives as below.
+            if (!whole && seg_start == 0 && i == n_tiles - 1 && (maybe_empty || cgm.span <= kChunk) &&
+                unit_parts(cgm) <= 3) {
+                // This warp holds the unit's first part (the unit started in
+                // its range and runs to the range end).  The unit's other
+                // parts usually end early in their warps' ranges, so at this
+                // warp's range end they may all have arrived.  Then this warp
+                // is the last: it merges its registers with their partials,
+                // loaded straight from global memory (one round trip for a
+                // unit over two warps), and writes the row -- no partial of
+                // its own, no arrival.  Otherwise it publishes and arrives as
+                // below.  (Only the first part of a unit of at most three
+                // parts does this: merge_regs reproduces merge_parts_smem's
+                // arithmetic for that case.)
                 int known = 0;
                 if (lane == 0) known = ld_acquire_gpu(p.counters + u) == unit_parts(cgm) - 1;
                 merged = __shfl_sync(kFull, known, 0) != 0;
@@ -1429,17 +1340,19 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                 const int d0 = kFp8 ? 16 * g : 8 * g;          // first run of dims
                 const int d1 = kFp8 ? 16 * g + 8 : 64 + 8 * g; // second run (8 dims each)
                 if (whole) {
-                    const float f = unit_bad ? 0.f : cvsc / lt[j];
+                    const float f = cvsc / lt[j];
                     __nv_bfloat16 *orow = p.out + (static_cast<int64_t>(C.r) * p.Hq + C.h * G + hd) * kD;
-                    uint4 r0v, r1v;
-                    r0v.x = pack_bf16x2(v[0] * f, v[1] * f);
-                    r0v.y = pack_bf16x2(v[2] * f, v[3] * f);
-                    r0v.z = pack_bf16x2(v[4] * f, v[5] * f);
-                    r0v.w = pack_bf16x2(v[6] * f, v[7] * f);
-                    r1v.x = pack_bf16x2(v[8] * f, v[9] * f);
-                    r1v.y = pack_bf16x2(v[10] * f, v[11] * f);
-                    r1v.z = pack_bf16x2(v[12] * f, v[13] * f);
-                    r1v.w = pack_bf16x2(v[14] * f, v[15] * f);
+                    uint4 r0v = make_uint4(0u, 0u, 0u, 0u), r1v = make_uint4(0u, 0u, 0u, 0u);
+                    if (!unit_bad) {                           // fail closed: zeros, whatever the data
+                        r0v.x = pack_bf16x2(v[0] * f, v[1] * f);
+                        r0v.y = pack_bf16x2(v[2] * f, v[3] * f);
+                        r0v.z = pack_bf16x2(v[4] * f, v[5] * f);
+                        r0v.w = pack_bf16x2(v[6] * f, v[7] * f);
+                        r1v.x = pack_bf16x2(v[8] * f, v[9] * f);
+                        r1v.y = pack_bf16x2(v[10] * f, v[11] * f);
+                        r1v.z = pack_bf16x2(v[12] * f, v[13] * f);
+                        r1v.w = pack_bf16x2(v[14] * f, v[15] * f);
+                    }
                     *reinterpret_cast<uint4 *>(orow + d0) = r0v;
                     *reinterpret_cast<uint4 *>(orow + d1) = r1v;
                 } else {
@@ -1478,7 +1391,6 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                     stage = __shfl_sync(kFull, last, 0) ? kChunkDue : kNone;
                 }
                 // at the range end the stage ring is idle: merge through it
-#if FKV_DEFER_MIDRANGE
                 if (stage != kNone && i < n_tiles - 1) {
                     // mid-range: the stream would stall for the merge, and a
                     // part ending just before this range's end can be the last
@@ -1491,15 +1403,12 @@ paged_decode_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap
                     def_vsc = cvsc;
                     stage = kNone;
                 }
-#endif
-                if (stage != kNone) merge_steps(stage, gm, C.r, C.h, cvsc, i == n_tiles - 1);
+                if (stage != kNone) merge_steps(stage, gm, C.r, C.h, cvsc);
             }
         }
         cursor_next(C, p);
     }
-#if FKV_DEFER_MIDRANGE
-    if (def_stage != kNone) merge_steps(def_stage, def_gm, def_r, def_h, def_vsc, true);
-#endif
+    if (def_stage != kNone) merge_steps(def_stage, def_gm, def_r, def_h, def_vsc);
     grid_dep_launch();
 }
 

@@ -383,3 +383,79 @@ def test_abort_equals_absent_under_whole_warp_schedule(orc):
     torch.cuda.synchronize()
     assert np.array_equal(full[keep].view(torch.int16).numpy(), out.cpu().view(torch.int16).numpy())
     assert_close(bf16_out(full), case.oracle(orc, abort_mask=am), "aborted middle request")
+
+
+def _spare_page_zero(case):
+    """Relabel so that physical page 0 is a spare page (listed by no request):
+    swap its contents and its id with one that is."""
+    used = set(case.indices.tolist())
+    if 0 in used:
+        s = next(x for x in range(case.P) if x not in used)
+        for pool in (case.kc, case.vc):
+            pool[[0, s]] = pool[[s, 0]]
+        case.indices = np.where(case.indices == 0, s, case.indices).astype(np.int32)
+    return case
+
+
+@pytest.mark.parametrize("kv", ["fp8", "bf16"])
+@pytest.mark.parametrize("S", [16, 64])
+def test_bad_page_rows_are_zero_over_nan_bytes(orc, kv, S):
+    """A page id outside the pool is replaced by page 0 for the copy and the
+    unit is marked bad; its row must be zeros even when page 0 holds NaN codes
+    (a short request whose unit one warp covers whole, and a long one split
+    over several warps), with no abort mask to catch them first."""
+    import fp8_paged_kv_decode_gb300 as fkv
+    case = _spare_page_zero(PagedCase(orc, 4, 32, 4, S, [150, 30000, 2000, 9000], kv=kv, seed=31, spare=4))
+    if case.fp8:
+        case.kc[0] = 0x7F
+        case.vc[0] = 0xFF
+    else:
+        case.kc[0] = 0x7FC0
+        case.vc[0] = 0xFFC0
+    ind = case.indices.copy()
+    ind[case.indptr[0]] = case.P + 7                    # request 0: one unit per KV head, one warp each
+    ind[case.indptr[1] + 100] = -3                      # request 1: units split over many warps
+    fkv.device_error(clear=True)
+    got = bf16_out(case.gpu(indices=ind))
+    ref = case.oracle(orc, indices=ind)
+    for r in (0, 1):
+        assert not ref[r].any()
+        assert np.array_equal(got[r], np.zeros_like(got[r])), r
+    assert_close(got, ref, "bad pages over NaN bytes")
+    assert fkv.device_error() & fkv.DEVERR_ATTN_PAGE
+
+
+@pytest.mark.parametrize("kv", ["fp8", "bf16"])
+def test_run_to_run_byte_identity(orc, kv):
+    """The same call repeated gives the same bytes, although which warp
+    merges a split unit, and whether it merges from its registers or through
+    shared memory, depends on when the unit's parts arrive: every merge folds
+    the parts in the same order with the same roundings.  The batch mixes
+    units over one warp, over a few (one merge level) and over many (two
+    levels); calls alternate with a write that evicts L2, so timings vary."""
+    import torch
+    case = PagedCase(orc, 12, 64, 8, 64, [20000, 9000, 3000, 15000, 500, 7000, 12000, 800, 25000, 4000, 6000, 1],
+                     kv=kv, seed=33)
+    assert_close(bf16_out(case.gpu()), case.oracle(orc), "byte-identity batch")
+    import fp8_paged_kv_decode_gb300 as fkv
+    q = dev(case.q, dtype=torch.bfloat16)
+    cdt = None if case.fp8 else torch.bfloat16
+    kt, vt = dev(case.kc, dtype=cdt), dev(case.vc, dtype=cdt)
+    ks = dev(case.k_scale) if case.fp8 else None
+    vs = dev(case.v_scale) if case.fp8 else None
+    ip, ix, sl = dev(case.indptr), dev(case.indices), dev(case.seq)
+    ws = fkv.alloc_workspace(case.B, case.Hq, case.Hkv, fkv.KV_FP8_E4M3 if case.fp8 else fkv.KV_BF16)
+    out = torch.empty((case.B, case.Hq, 128), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(64 * 2 ** 20, dtype=torch.float32, device="cuda")     # 256 MB > L2
+    first = None
+    for it in range(40):
+        if it % 2:
+            flush.fill_(float(it))
+        out.fill_(float("nan"))
+        fkv.paged_decode_attn(q, kt, vt, ip, ix, sl, case.sm, out, ws, k_scale=ks, v_scale=vs)
+        torch.cuda.synchronize()
+        got = out.view(torch.int16).cpu().numpy().copy()
+        if first is None:
+            first = got
+        else:
+            assert np.array_equal(got, first), "call %d differs from the first" % it
