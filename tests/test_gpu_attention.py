@@ -425,18 +425,26 @@ def test_bad_page_rows_are_zero_over_nan_bytes(orc, kv, S):
     assert fkv.device_error() & fkv.DEVERR_ATTN_PAGE
 
 
-@pytest.mark.parametrize("kv", ["fp8", "bf16"])
-def test_run_to_run_byte_identity(orc, kv):
+def _identity_case(orc, shape, kv):
+    if shape == "mixed":        # units over one warp, a few (one merge level), many (two levels)
+        return PagedCase(orc, 12, 64, 8, 64, [20000, 9000, 3000, 15000, 500, 7000, 12000, 800, 25000, 4000, 6000, 1],
+                         kv=kv, seed=33)
+    # 160 requests of 16-token pages: the plan kernel's table and the two-warp CTA
+    seq = np.random.default_rng(34).integers(1, 3000, 160)
+    return PagedCase(orc, 160, 32, 4, 16, seq, kv=kv, seed=34)
+
+
+@pytest.mark.parametrize("kv,shape", [("fp8", "mixed"), ("bf16", "mixed"), ("fp8", "plan")])
+def test_run_to_run_byte_identity(orc, kv, shape):
     """The same call repeated gives the same bytes, although which warp
     merges a split unit, and whether it merges from its registers or through
     shared memory, depends on when the unit's parts arrive: every merge folds
-    the parts in the same order with the same roundings.  The batch mixes
-    units over one warp, over a few (one merge level) and over many (two
-    levels); calls alternate with a write that evicts L2, so timings vary."""
+    the parts in the same order with the same roundings.  Calls alternate
+    with a write that evicts L2, so timings vary."""
     import torch
-    case = PagedCase(orc, 12, 64, 8, 64, [20000, 9000, 3000, 15000, 500, 7000, 12000, 800, 25000, 4000, 6000, 1],
-                     kv=kv, seed=33)
-    assert_close(bf16_out(case.gpu()), case.oracle(orc), "byte-identity batch")
+    case = _identity_case(orc, shape, kv)
+    if shape == "mixed":
+        assert_close(bf16_out(case.gpu()), case.oracle(orc), "byte-identity batch")
     import fp8_paged_kv_decode_gb300 as fkv
     q = dev(case.q, dtype=torch.bfloat16)
     cdt = None if case.fp8 else torch.bfloat16
