@@ -19,8 +19,9 @@
 //     resident CTAs): the concatenation of all units' tiles is cut into equal
 //     contiguous ranges, one per computing warp (split-KV with even load
 //     across the lognormal context mix); a small batch instead gives each
-//     unit whole warps of its own (a separate kernel instance, chosen by the
-//     host from a bound on the batch's tiles).  For batches of up to 128
+//     unit whole warps of its own (the kernel instance for batches of up to
+//     64 requests, whose warps test the live requests' tiles and fall back
+//     to the even split).  For batches of up to 128
 //     requests each warp finds its own range from the inputs and starts its
 //     copies before the plan kernel has finished.  Each warp streams its tiles
 //     through a private ring of shared-memory stages filled by 128B-swizzled
@@ -35,8 +36,11 @@
 //     (o, m, l), and the last of the unit's warps to arrive (an atomic
 //     counter, no waiting) merges the partials with a log-sum-exp rescale
 //     (two levels for units split over many warps), fetching them with 1-D
-//     bulk copies into its idle stage ring at the end of its range.  Rows of requests with no tiles (aborted,
-//     empty, malformed) are zero-filled by the warps, one request each.
+//     bulk copies into its idle stage ring at the end of its range.  The
+//     merge's arithmetic is fixed (merge_parts_smem), so the bytes of a row
+//     do not depend on which warp merges it or when.  Rows of requests with
+//     no tiles (aborted, empty, malformed) are zero-filled by the warps, one
+//     request each.
 #include <cudaTypedefs.h>
 
 #include <cmath>
