@@ -258,8 +258,13 @@ FKV_API size_t paged_decode_attn_workspace_size(int32_t batch, int32_t num_q_hea
  * Fail closed: a request that is aborted, has a malformed CSR row (indptr[r]
  * < 0, indptr[r+1] < indptr[r] or indptr[r+1] > nnz), has seq_lens[r] <= 0,
  * has more tokens than its pages hold, or whose pages include an id outside
- * [0, num_pages), gets an all-zero output row; its pages are not read (an
- * out-of-range id is never dereferenced) and no other row is affected.
+ * [0, num_pages), gets an all-zero output row, and no other row is affected.
+ * The pages of the first four kinds are not read.  An id outside the pool is
+ * never dereferenced: that tile is copied from page 0 instead, and the row is
+ * written as zeros whatever those bytes hold (FKV_DEVERR_ATTN_PAGE is set).
+ * Deterministic: the same call gives the same bytes every time (the split
+ * over warps depends only on the live requests, and the merge of a split
+ * (request, KV head) does not depend on which warp performs it or when).
  * Supported: head_dim 128, page_size in {16, 32, 64, 128}, group size
  * G = num_q_heads / num_kv_heads in 1..8, or above 8 when G splits into R
  * equal groups of at most 8 with R a power of two up to 8 (10, 12, 16, 24,
