@@ -276,6 +276,25 @@ class Step:
                                    v_scale=self.v_scale if self.fp8 else None,
                                    abort_mask=self.mask if with_mask else None)
 
+    def repeat_identical(self, calls=8):
+        """Bytes of the attention output over ``calls`` repeated calls on the
+        step's final cache and mask, between writes that evict L2: True if
+        every call gave the same bytes."""
+        torch = self.torch
+        flush = torch.empty(64 * 2 ** 20, dtype=torch.float32, device=self.device)
+        ref = None
+        same = True
+        for i in range(calls):
+            flush.fill_(float(i))
+            self.attend(True)
+            torch.cuda.synchronize(self.device)
+            got = self.out.view(torch.int16).clone()
+            if ref is None:
+                ref = got
+            else:
+                same = same and bool(torch.equal(got, ref))
+        return same
+
     def launches_per_step(self, with_check=True):
         return 1 + self.fkv.kernels_per_call("paged_decode_attn")   # append (+ check), attention
 
@@ -1032,6 +1051,7 @@ def main():
                 "steps": e2e_steps},
         "gpu_launches": args.steps * fp8.launches_per_step(),
         "clocks": sampler.summary(),
+        "attention_repeat_bytes_identical": fp8.repeat_identical(),
     }
 
     if not args.skip_extras and args.kv == "fp8":
