@@ -29,7 +29,7 @@ __all__ = [
     "paged_decode_attn_workspace_size",
     "alloc_workspace",
     "paged_decode_attn_noalloc",
-    "device_error", "kernels_per_call", "EXPORTED_SYMBOLS",
+    "device_error", "kernels_per_call", "selftest_wait", "EXPORTED_SYMBOLS",
 ]
 
 KV_FP8_E4M3 = 0
@@ -44,7 +44,7 @@ EXPORTED_SYMBOLS = (
     "fkv_status_string", "kv_append_fp8", "kv_append_bf16", "kv_calibrate_scales", "kv_page_tag_check",
     "kv_append_fp8_tag_check", "kv_append_bf16_tag_check", "kv_page_realloc",
     "paged_decode_attn_workspace_size", "paged_decode_attn", "paged_decode_attn_noalloc", "fkv_device_error",
-    "fkv_kernels_per_call",
+    "fkv_kernels_per_call", "fkv_selftest_wait",
 )
 ERR_SCRATCH_LIMIT = 4
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -107,6 +107,8 @@ def load_library():
         lib.fkv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         lib.fkv_kernels_per_call.restype = i32
         lib.fkv_kernels_per_call.argtypes = [ctypes.c_char_p]
+        lib.fkv_selftest_wait.restype = ctypes.c_int
+        lib.fkv_selftest_wait.argtypes = [ctypes.c_uint64, i32, P, P]
         _lib = lib
         return lib
 
@@ -357,3 +359,18 @@ def device_error(clear: bool = True) -> int:
 
 def kernels_per_call(entry_point: str) -> int:
     return int(load_library().fkv_kernels_per_call(entry_point.encode()))
+
+
+def selftest_wait(limit_ns: int, complete: bool = False, result=None, stream=None):
+    """Run the failure path of the kernels' bounded waits on the GPU: one
+    block waits, with the library's two wait helpers, on an mbarrier that
+    nothing completes (``complete=False``) and gives up after ``limit_ns``,
+    setting DEVERR_TIMEOUT; with ``complete=True`` the waits return at once.
+    ``result``: None or a CUDA uint32 tensor of 2 (1 = the wait saw the
+    barrier complete, 0 = it gave up, per warp)."""
+    if result is not None:
+        _dev(result)
+        import torch
+        _need(result.dtype in (torch.uint32, torch.int32) and result.numel() >= 2, "result: 2 x 32-bit")
+    _raise(load_library().fkv_selftest_wait(int(limit_ns), 1 if complete else 0, _ptr(result), _stream(stream)),
+           "fkv_selftest_wait")

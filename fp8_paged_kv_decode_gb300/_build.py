@@ -15,7 +15,8 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 LIB = os.path.join(PKG, "libfkv.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["fkv_api.cu", "kv_append.cu", "tag_check.cu", "decode_attn.cu", "decode_attn_noalloc.cu", "page_realloc.cu", "kv_calibrate.cu"]
+SOURCES = ["fkv_api.cu", "kv_append.cu", "tag_check.cu", "decode_attn.cu", "decode_attn_noalloc.cu", "page_realloc.cu",
+           "kv_calibrate.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -339,6 +339,22 @@ FKV_API fkv_status fkv_device_error(uint32_t *flags, int32_t clear);
 /* Number of kernels one call launches (for launch accounting). */
 FKV_API int32_t fkv_kernels_per_call(const char *entry_point);
 
+/*
+ * fkv_selftest_wait -- run the failure path of the kernels' bounded waits
+ * (diagnostic; the pages have no counterpart).  Every wait in the library's
+ * kernels is on an mbarrier that a copy or another warp completes, and gives
+ * up after a time limit, recording FKV_DEVERR_TIMEOUT instead of hanging.
+ * This launches one block whose two warps run those two wait helpers (the
+ * spinning and the sleeping one) on an mbarrier that nothing completes: each
+ * gives up after limit_ns nanoseconds, sets FKV_DEVERR_TIMEOUT and the kernel
+ * ends normally.  With complete != 0 the block completes the barrier first
+ * and both waits return at once (no error bit).  result: NULL, or a device
+ * uint32[2] receiving 1 (the wait saw the barrier complete) or 0 (it gave
+ * up) per warp.  limit_ns above 10 s returns FKV_ERR_INVALID_ARG.
+ * Asynchronous on `stream`; read the outcome with fkv_device_error.
+ */
+FKV_API fkv_status fkv_selftest_wait(uint64_t limit_ns, int32_t complete, uint32_t *result, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -83,3 +83,4 @@ def test_host_validation_without_gpu(lib_path):
                                  0.1, None, None, 0, None) == 1     # group 16 (two groups of 8): null pointers
     assert lib.paged_decode_attn(None, 2, 8, None, None, 0, None, None, 4, 2, 16, 128, None, None, 0, None, None,
                                  -1.0, None, None, 0, None) == 1    # sm_scale must be positive
+    assert lib.fkv_selftest_wait(10_000_000_001, 0, None, None) == 1     # more than 10 s of waiting
