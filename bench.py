@@ -589,11 +589,13 @@ def barrier():
 
 
 def max_over_ranks(x):
+    """The largest of every rank's x (the job's time is its slowest rank's)."""
     if _PG is None:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

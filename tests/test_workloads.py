@@ -73,9 +73,12 @@ def _gloo_worker(rank, world, port, q):
     t = torch.zeros(64, dtype=torch.int64)
     t[mine] = 1
     dist.all_reduce(t)
-    # the bench's timing reduction: max over ranks of the per-rank time
-    ms = torch.tensor([10.0 + rank], dtype=torch.float64)
-    dist.all_reduce(ms, op=dist.ReduceOp.MAX)
+    # the bench's own barrier and timing reduction: max over ranks of the
+    # per-rank time
+    import bench
+    bench._PG = True
+    bench.barrier()
+    ms = bench.max_over_ranks(10.0 + rank)
     q.put((rank, t.tolist(), float(ms)))
     dist.destroy_process_group()
 
@@ -142,3 +145,16 @@ def test_subset_batch_keeps_the_first_requests():
     assert W.subset_batch(db, 0).wl.batch == 0
     with pytest.raises(ValueError):
         W.subset_batch(db, db.wl.batch + 1)
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Launched as two ranks, the reference arm's rank 1 exits 0 without work
+    or output (rank 0 alone runs the oracle and prints the line)."""
+    import subprocess
+    import sys
+    env = dict(os.environ, RANK="1", LOCAL_RANK="1", WORLD_SIZE="2", MASTER_ADDR="127.0.0.1")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
