@@ -98,33 +98,9 @@ __device__ __forceinline__ int64_t slot_offset(int64_t slot, int32_t num_pages, 
     return ((page * num_kv_heads + by) * page_size + off) * kHeadDim;
 }
 
-// One thread's share of the FP8 append in block (bx, by).
-__device__ __forceinline__ void append_fp8_part(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
-                                                const int64_t *__restrict__ slots, int64_t n_tokens,
-                                                const float *__restrict__ k_scale, const float *__restrict__ v_scale,
-                                                uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
-                                                int32_t num_pages, int32_t num_kv_heads, int32_t page_size,
-                                                int32_t page_shift, uint32_t *err, unsigned bx, unsigned by) {
-    const int64_t n = token_of(n_tokens, bx);
-    if (n < 0) return;
-    const int h = by;
-    const int sub = threadIdx.x % kThreadsPerToken;
-    const bool is_v = sub >= kThreadsPerRow;
-    const int chunk = sub % kThreadsPerRow;
-    // 16 bf16 = two uint4 per thread; row (n, h) starts at uint4 index (n*Hkv + h) * 16
-    const uint4 *src = (is_v ? v_new : k_new) + (n * num_kv_heads + h) * (kHeadDim / 8) + chunk * 2;
-    // the row, its scale and its slot are independent loads, all in flight at
-    // once (1.4 % faster on a bulk write than loading the row after the slot
-    // has come back; placing the slot's use after the quotient instead, at
-    // the store, measured 0.7 % slower than that).  Streaming hints on both
-    // sides (the bf16 input is read once, the codes are not read back by this
-    // kernel): 4.8 % faster on a bulk write than plain loads and stores, while
-    // either hint alone is not
-    const uint4 r0 = __ldcs(src), r1 = __ldcs(src + 1);
-    const float b = __ldg((is_v ? v_scale : k_scale) + h);
-    const int64_t slot = __ldg(slots + n);
-    const int64_t dst_off = slot_offset(slot, num_pages, num_kv_heads, page_size, page_shift, err, by);
-    if (dst_off < 0) return;
+// The e4m3 codes of one thread's 16 bf16 elements (two uint4 of the row, in
+// order) divided by the scale b, as one uint4 (code k in byte k).
+__device__ __forceinline__ uint4 encode16(const uint4 r0, const uint4 r1, float b) {
     const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
     uint32_t big = 0;                                          // largest |x| bit patterns, per half
 #pragma unroll
@@ -156,8 +132,38 @@ __device__ __forceinline__ void append_fp8_part(const uint4 *__restrict__ k_new,
             packed[p] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
         }
     }
+    return make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
+
+// One thread's share of the FP8 append in block (bx, by).
+__device__ __forceinline__ void append_fp8_part(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                                                const int64_t *__restrict__ slots, int64_t n_tokens,
+                                                const float *__restrict__ k_scale, const float *__restrict__ v_scale,
+                                                uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
+                                                int32_t num_pages, int32_t num_kv_heads, int32_t page_size,
+                                                int32_t page_shift, uint32_t *err, unsigned bx, unsigned by) {
+    const int64_t n = token_of(n_tokens, bx);
+    if (n < 0) return;
+    const int h = by;
+    const int sub = threadIdx.x % kThreadsPerToken;
+    const bool is_v = sub >= kThreadsPerRow;
+    const int chunk = sub % kThreadsPerRow;
+    // 16 bf16 = two uint4 per thread; row (n, h) starts at uint4 index (n*Hkv + h) * 16
+    const uint4 *src = (is_v ? v_new : k_new) + (n * num_kv_heads + h) * (kHeadDim / 8) + chunk * 2;
+    // the row, its scale and its slot are independent loads, all in flight at
+    // once (1.4 % faster on a bulk write than loading the row after the slot
+    // has come back; placing the slot's use after the quotient instead, at
+    // the store, measured 0.7 % slower than that).  Streaming hints on both
+    // sides (the bf16 input is read once, the codes are not read back by this
+    // kernel): 4.8 % faster on a bulk write than plain loads and stores, while
+    // either hint alone is not
+    const uint4 r0 = __ldcs(src), r1 = __ldcs(src + 1);
+    const float b = __ldg((is_v ? v_scale : k_scale) + h);
+    const int64_t slot = __ldg(slots + n);
+    const int64_t dst_off = slot_offset(slot, num_pages, num_kv_heads, page_size, page_shift, err, by);
+    if (dst_off < 0) return;
     uint8_t *dst = (is_v ? v_cache : k_cache) + dst_off + chunk * kElemsPerThread;
-    __stcs(reinterpret_cast<uint4 *>(dst), make_uint4(packed[0], packed[1], packed[2], packed[3]));
+    __stcs(reinterpret_cast<uint4 *>(dst), encode16(r0, r1, b));
 }
 
 __global__ void __launch_bounds__(kBlock, FKV_APPEND_MIN_BLOCKS)

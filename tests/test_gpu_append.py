@@ -24,25 +24,31 @@ def _run_fp8(orc, P, Hkv, S, kf, vf, slots, ks, vs, seed=0):
     return kt.cpu().numpy(), vt.cpu().numpy(), kc, vc, kc0, vc0
 
 
-def test_append_fp8_bitexact_whole_pool(orc):
+@pytest.mark.parametrize("P,Hkv,S,N", [(64, 4, 16, 300),
+                                       # a bulk write (20 504 blocks), with a ragged last group
+                                       (2600, 8, 16, 41001)])
+def test_append_fp8_bitexact_whole_pool(orc, P, Hkv, S, N):
     import fp8_paged_kv_decode_gb300 as fkv
-    rng = np.random.default_rng(1)
-    P, Hkv, S, N = 64, 4, 16, 300
+    rng = np.random.default_rng(1 + N)
     slots = rng.choice(P * S, size=N, replace=False).astype(np.int64)
     slots[::17] = -1                                   # padding tokens
+    outside = N > 1000
+    if outside:                                        # slots past the pool: skipped and flagged
+        slots[5] = P * S + 3
+        slots[-2] = 2 * P * S
     kf = (rng.standard_normal((N, Hkv, 128)) * np.exp2(rng.integers(-8, 8, (N, Hkv, 1)))).astype(np.float32)
     vf = rng.standard_normal((N, Hkv, 128)).astype(np.float32)
-    ks = np.float32([0.003, 0.5, 1.0, 7.0])
-    vs = np.float32([0.01, 0.02, 0.03, 0.04])
+    ks = np.resize(np.float32([0.003, 0.5, 1.0, 7.0]), Hkv)
+    vs = np.resize(np.float32([0.01, 0.02, 0.03, 0.04]), Hkv)
     fkv.device_error(clear=True)
     gk, gv, kc, vc, kc0, _ = _run_fp8(orc, P, Hkv, S, kf, vf, slots, ks, vs)
     assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
     # bytes outside the written slots are untouched
     written = np.zeros(P * S, bool)
-    written[slots[slots >= 0]] = True
+    written[slots[(slots >= 0) & (slots < P * S)]] = True
     untouched = ~written.reshape(P, S)
     assert np.array_equal(gk.transpose(0, 2, 1, 3)[untouched], kc0.transpose(0, 2, 1, 3)[untouched])
-    assert fkv.device_error() == 0
+    assert fkv.device_error() == (fkv.DEVERR_APPEND_SLOT if outside else 0)
 
 
 def test_append_fp8_special_values(orc):
