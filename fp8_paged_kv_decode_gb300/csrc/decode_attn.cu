@@ -93,7 +93,7 @@ constexpr uint32_t kFull = 0xffffffffu;
 #define FKV_ALIGNED_MIN_TILES 2
 #endif
 #ifndef FKV_MIN_TILES_PER_WARP
-#define FKV_MIN_TILES_PER_WARP 8
+#define FKV_MIN_TILES_PER_WARP 12
 #endif
 constexpr int kNone = 0, kFinalDue = 1, kChunkDue = 2;   // merge duties of a warp
 constexpr int kChunk = FKV_MERGE_CHUNK;  // parts merged per first-level merge of a long unit

@@ -287,16 +287,16 @@ def test_batch_beyond_plan_smem_table(orc):
 @pytest.mark.parametrize("seq,abort", [
     ([1, 64, 65], None),
     ([30000, 100, 0, 5000, 700], [0, 1, 0, 0, 0]),
-    ([67648, 67648], None),
-    ([67712, 67712], None),
+    ([106304, 106304], None),
+    ([106368, 106368], None),
 ], ids=["one_tile_units", "mixed", "whole_warp_max", "even_split_min"])
 def test_small_batch_schedules(orc, kv, S, seq, abort):
     """Small batches give every (request, KV head) unit whole warps: units of
     one or two tiles get one warp and need no merge, long ones are split
     evenly over their own warps, and empty or aborted requests get none.
-    Two requests of 1057 tiles per head are the most a 152-SM part schedules
-    this way with FP8 (7 tiles per warp); one tile more per head takes the
-    even split of the batch's tiles.  Page size 16 runs the producer-warp
+    Two requests of 1661 tiles per head are the most a 152-SM part schedules
+    this way (11 tiles per warp, one below the even split's minimum of 12);
+    one tile more per head takes the even split of the batch's tiles.  Page size 16 runs the producer-warp
     CTA, 64 the single-warp one."""
     B = len(seq)
     case = PagedCase(orc, B, 16, 2, S, seq, kv=kv, seed=sum(seq) + S + (kv == "bf16"))
